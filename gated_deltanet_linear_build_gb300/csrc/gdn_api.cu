@@ -1,0 +1,168 @@
+// C ABI of the GDN hot path: host-side argument validation, then the kernel
+// launchers. Nothing here allocates device memory or synchronises.
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+std::mutex g_err_mu;
+std::string g_err_text;
+constexpr int kConvTaps = 4;
+
+bool head_dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+}  // namespace
+
+void set_cuda_error(cudaError_t e) {
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  g_err_text = cudaGetErrorName(e);
+  g_err_text += ": ";
+  g_err_text += cudaGetErrorString(e);
+}
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status_t s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: shape or option not implemented";
+    case GDN_ERR_ALIGNMENT: return "GDN_ERR_ALIGNMENT: pointer or stride not 16-byte aligned";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace or capacity too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: CUDA call failed";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: bounded device wait gave up";
+  }
+  return "GDN: unknown status";
+}
+
+const char* gdn_last_cuda_error_string(void) {
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  return g_err_text.c_str();
+}
+
+gdn_status_t gdn_build_conv_chunks(const int32_t* cu_seqlens, int32_t num_seqs,
+                                   int32_t chunk_tokens, gdn_conv_chunk_t* chunks,
+                                   int32_t capacity, int32_t* num_chunks,
+                                   int32_t* device_status, void* stream) {
+  if (!cu_seqlens || !num_chunks || num_seqs < 0 || capacity < 0) return GDN_ERR_INVALID_ARG;
+  if (chunk_tokens < kConvTaps - 1) return GDN_ERR_INVALID_ARG;
+  if (capacity > 0 && !chunks) return GDN_ERR_INVALID_ARG;
+  if (chunks && !aligned16(chunks)) return GDN_ERR_ALIGNMENT;
+  return launch_build_chunks(cu_seqlens, num_seqs, chunk_tokens, chunks, capacity, num_chunks,
+                             device_status, static_cast<cudaStream_t>(stream));
+}
+
+static gdn_status_t check_conv_common(const void* x, int64_t x_stride, const void* w,
+                                      const void* bias, void* conv_state, int32_t C, int32_t K,
+                                      int32_t silu, void* y) {
+  if (!x || !w || !conv_state || !y) return GDN_ERR_INVALID_ARG;
+  if (C <= 0 || x_stride < C || (silu != 0 && silu != 1)) return GDN_ERR_INVALID_ARG;
+  if (K != kConvTaps) return GDN_ERR_UNSUPPORTED;
+  if (C % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (x_stride % 8 != 0) return GDN_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(conv_state) || !aligned16(y) ||
+      (bias && !aligned16(bias)))
+    return GDN_ERR_ALIGNMENT;
+  return GDN_OK;
+}
+
+gdn_status_t gdn_causal_conv1d_fwd(const void* x, int64_t x_stride, const void* w,
+                                   const void* bias, void* conv_state,
+                                   const uint8_t* has_initial_state,
+                                   const int32_t* cu_seqlens,
+                                   const gdn_conv_chunk_t* chunks,
+                                   const int32_t* num_chunks, int32_t max_chunks,
+                                   int32_t T, int32_t C, int32_t K, int32_t N,
+                                   int32_t silu, void* y, void* stream) {
+  if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
+  if ((chunks == nullptr) != (num_chunks == nullptr)) return GDN_ERR_INVALID_ARG;
+  if (chunks && max_chunks < 0) return GDN_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return GDN_OK;
+  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  gdn_status_t rc = check_conv_common(x, x_stride, w, bias, conv_state, C, K, silu, y);
+  if (rc != GDN_OK) return rc;
+  if (chunks && !aligned16(chunks)) return GDN_ERR_ALIGNMENT;
+  const int32_t units = chunks ? max_chunks : N;
+  return launch_conv_fwd(x, x_stride, w, bias, conv_state, has_initial_state, cu_seqlens, chunks,
+                         num_chunks, units, T, C, N, silu, y, static_cast<cudaStream_t>(stream));
+}
+
+gdn_status_t gdn_causal_conv1d_update(const void* x, int64_t x_stride, const void* w,
+                                      const void* bias, void* conv_state, int32_t N,
+                                      int32_t C, int32_t K, int32_t silu, void* y,
+                                      void* stream) {
+  if (N < 0) return GDN_ERR_INVALID_ARG;
+  if (N == 0) return GDN_OK;
+  gdn_status_t rc = check_conv_common(x, x_stride, w, bias, conv_state, C, K, silu, y);
+  if (rc != GDN_OK) return rc;
+  return launch_conv_update(x, x_stride, w, bias, conv_state, N, C, silu, y,
+                            static_cast<cudaStream_t>(stream));
+}
+
+static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_stride,
+                                       const void* v, int64_t v_stride, const float* a,
+                                       const float* b, const float* S, const void* o,
+                                       int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                       int32_t qk_l2norm) {
+  if (!q || !k || !v || !a || !b || !S || !o) return GDN_ERR_INVALID_ARG;
+  if (Hk <= 0 || Hv <= 0 || (qk_l2norm != 0 && qk_l2norm != 1)) return GDN_ERR_INVALID_ARG;
+  if (Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
+  if (qk_stride < (int64_t)Hk * dk || v_stride < (int64_t)Hv * dv) return GDN_ERR_INVALID_ARG;
+  if (qk_stride % 8 != 0 || v_stride % 8 != 0) return GDN_ERR_ALIGNMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(o))
+    return GDN_ERR_ALIGNMENT;
+  return GDN_OK;
+}
+
+gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stride,
+                                   const void* v, int64_t v_stride, const float* a,
+                                   const float* b, float* S, void* o, int32_t N,
+                                   int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                   int32_t qk_l2norm, void* stream) {
+  if (N < 0) return GDN_ERR_INVALID_ARG;
+  if (N == 0) return GDN_OK;
+  gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
+                                       qk_l2norm);
+  if (rc != GDN_OK) return rc;
+  if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
+  return launch_delta_decode(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv,
+                             qk_l2norm, static_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv, int32_t dk,
+                                             int32_t dv, int32_t chunk) {
+  return prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
+}
+
+gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
+                                            const void* v, int64_t v_stride,
+                                            const float* a, const float* b,
+                                            const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                            float* S, const uint8_t* has_initial_state,
+                                            void* o, int32_t Hk, int32_t Hv, int32_t dk,
+                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
+  if (chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if (T == 0 || N == 0) return GDN_OK;
+  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
+                                       qk_l2norm);
+  if (rc != GDN_OK) return rc;
+  if (dk != dv) return GDN_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
+  return launch_delta_prefill(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
+                              has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                              static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

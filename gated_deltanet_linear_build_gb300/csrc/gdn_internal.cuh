@@ -1,0 +1,98 @@
+// Internal helpers shared by the GDN CUDA translation units (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// ---------------------------------------------------------------------------
+// BF16 <-> float32 on packed 32-bit words (two BF16 values, element 0 in the
+// low half). Widening is exact; narrowing rounds to nearest even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// 8 BF16 values (one 16-byte vector) -> 8 floats.
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  f[0] = bf16lo(u.x); f[1] = bf16hi(u.x);
+  f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
+  f[4] = bf16lo(u.z); f[5] = bf16hi(u.z);
+  f[6] = bf16lo(u.w); f[7] = bf16hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 u;
+  u.x = pack_bf16x2(f[0], f[1]);
+  u.y = pack_bf16x2(f[2], f[3]);
+  u.z = pack_bf16x2(f[4], f[5]);
+  u.w = pack_bf16x2(f[6], f[7]);
+  return u;
+}
+
+// Read-only 16-byte global load (non-coherent path; inputs are never written
+// by the kernel that reads them).
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// Host-side helpers
+// ---------------------------------------------------------------------------
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Records the CUDA error text for gdn_last_cuda_error_string().
+void set_cuda_error(cudaError_t e);
+
+inline gdn_status_t check_launch() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_cuda_error(e);
+    return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
+}
+
+// Launchers implemented in the kernel translation units. They assume their
+// arguments were validated by the C ABI layer.
+gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
+                                 gdn_conv_chunk_t* chunks, int32_t capacity,
+                                 int32_t* num_chunks, int32_t* status, cudaStream_t st);
+
+gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, const void* bias,
+                             void* conv_state, const uint8_t* has_init, const int32_t* cu,
+                             const gdn_conv_chunk_t* chunks, const int32_t* num_chunks,
+                             int32_t units, int32_t T, int32_t C, int32_t N, int32_t silu,
+                             void* y, cudaStream_t st);
+
+gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
+                                const void* bias, void* conv_state, int32_t N, int32_t C,
+                                int32_t silu, void* y, cudaStream_t st);
+
+gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride,
+                                 const void* v, int64_t v_stride, const float* a,
+                                 const float* b, float* S, void* o, int32_t N, int32_t Hk,
+                                 int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
+                                 cudaStream_t st);
+
+size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
+                               int32_t chunk);
+
+gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_stride,
+                                  const void* v, int64_t v_stride, const float* a,
+                                  const float* b, const int32_t* cu, int32_t N, int32_t T,
+                                  float* S, const uint8_t* has_init, void* o, int32_t Hk,
+                                  int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
+                                  int32_t qk_l2norm, void* workspace, cudaStream_t st);
+
+}  // namespace gdn

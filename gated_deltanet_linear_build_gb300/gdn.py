@@ -1,0 +1,188 @@
+"""Python binding of the GDN C ABI (``include/gdn.h``), via ctypes.
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream of PyTorch to the library entry point of the same name
+and raises ``GdnError`` on a non-zero status. No arithmetic of the method
+happens here, and there is no fallback: if ``libgdn_gb300.so`` is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+GDN_OK = 0
+GDN_ERR_INVALID_ARG = -1
+GDN_ERR_UNSUPPORTED = -2
+GDN_ERR_ALIGNMENT = -3
+GDN_ERR_WORKSPACE = -4
+GDN_ERR_CUDA = -5
+GDN_ERR_TIMEOUT = -6
+
+# Every symbol that include/gdn.h declares.
+EXPORTED_SYMBOLS = (
+    "gdn_build_conv_chunks",
+    "gdn_causal_conv1d_fwd",
+    "gdn_causal_conv1d_update",
+    "gdn_delta_rule_decode",
+    "gdn_delta_rule_prefill_workspace_size",
+    "gdn_delta_rule_prefill_chunked",
+    "gdn_status_string",
+    "gdn_last_cuda_error_string",
+)
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        text = _LIB.gdn_status_string(status).decode() if _LIB is not None else str(status)
+        if status == GDN_ERR_CUDA and _LIB is not None:
+            text += " (" + _LIB.gdn_last_cuda_error_string().decode() + ")"
+        super().__init__(f"{fn}: {text}")
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+
+_SIGNATURES = {
+    "gdn_build_conv_chunks": (ctypes.c_int, [_P, _I32, _I32, _P, _I32, _P, _P, _P]),
+    "gdn_causal_conv1d_fwd": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _I32,
+                                             _I32, _I32, _I32, _I32, _I32, _P, _P]),
+    "gdn_causal_conv1d_update": (ctypes.c_int, [_P, _I64, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                                _P, _P]),
+    "gdn_delta_rule_decode": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P, _I32, _I32,
+                                             _I32, _I32, _I32, _I32, _P]),
+    "gdn_delta_rule_prefill_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I32, _I32,
+                                                                _I32]),
+    "gdn_delta_rule_prefill_chunked": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _I32,
+                                                      _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                                      _I32, _I32, _P, ctypes.c_size_t, _P]),
+    "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gdn_last_cuda_error_string": (ctypes.c_char_p, []),
+}
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the shared library (once) and declare its signatures."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"GDN CUDA library not built: {path} is missing "
+                           "(run __graft_entry__.build() or python -m "
+                           "gated_deltanet_linear_build_gb300.build)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _lib():
+    return _LIB if _LIB is not None else load_library()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, fn: str):
+    if rc != GDN_OK:
+        raise GdnError(rc, fn)
+
+
+# ----------------------------------------------------------------------------
+# Entry points (same names as the C ABI, without the gdn_ prefix)
+# ----------------------------------------------------------------------------
+
+def build_conv_chunks(cu_seqlens, chunks, num_chunks, *, chunk_tokens: int = 8,
+                      device_status=None, stream=None):
+    """Descriptors of the exact (sequence, chunk) dispatch.
+
+    cu_seqlens int32 [N+1]; chunks int32 [capacity, 4] (output); num_chunks
+    int32 [1] (output); device_status int32 [1] or None.
+    """
+    n = cu_seqlens.numel() - 1
+    rc = _lib().gdn_build_conv_chunks(_ptr(cu_seqlens), n, chunk_tokens, _ptr(chunks),
+                                      chunks.shape[0] if chunks is not None else 0,
+                                      _ptr(num_chunks), _ptr(device_status), _stream(stream))
+    _check(rc, "gdn_build_conv_chunks")
+
+
+def causal_conv1d_fwd(x, w, bias, conv_state, has_initial_state, cu_seqlens, y, *,
+                      chunks=None, num_chunks=None, silu: bool = True, stream=None):
+    """Varlen causal conv prefill. x [T, C] (row stride x.stride(0)), w [C, 4],
+    bias [C] or None, conv_state [N, C, 3], has_initial_state uint8 [N] or None,
+    y [T, C]. chunks/num_chunks as built by build_conv_chunks, or both None for
+    whole-sequence dispatch."""
+    T, C = x.shape
+    N = cu_seqlens.numel() - 1
+    rc = _lib().gdn_causal_conv1d_fwd(
+        _ptr(x), x.stride(0), _ptr(w), _ptr(bias), _ptr(conv_state), _ptr(has_initial_state),
+        _ptr(cu_seqlens), _ptr(chunks), _ptr(num_chunks),
+        chunks.shape[0] if chunks is not None else 0, T, C, w.shape[1], N, int(silu), _ptr(y),
+        _stream(stream))
+    _check(rc, "gdn_causal_conv1d_fwd")
+
+
+def causal_conv1d_update(x, w, bias, conv_state, y, *, silu: bool = True, stream=None):
+    """One decode token per sequence: x [N, C], conv_state [N, C, 3], y [N, C]."""
+    N, C = x.shape
+    rc = _lib().gdn_causal_conv1d_update(_ptr(x), x.stride(0), _ptr(w), _ptr(bias),
+                                         _ptr(conv_state), N, C, w.shape[1], int(silu),
+                                         _ptr(y), _stream(stream))
+    _check(rc, "gdn_causal_conv1d_update")
+
+
+def delta_rule_decode(q, k, v, a, b, S, o, *, qk_l2norm: bool = False, stream=None):
+    """Decode update. q, k [N, Hk, dk] (token stride q.stride(0), heads
+    contiguous), v [N, Hv, dv], a, b [N, Hv] float32, S [N, Hv, dv, dk] float32
+    (in place), o [N, Hv, dv]."""
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    assert k.stride(0) == q.stride(0), "q and k share one token stride"
+    rc = _lib().gdn_delta_rule_decode(_ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0),
+                                      _ptr(a), _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk, dv,
+                                      int(qk_l2norm), _stream(stream))
+    _check(rc, "gdn_delta_rule_decode")
+
+
+def delta_rule_prefill_workspace_size(T: int, N: int, Hv: int, dk: int, dv: int,
+                                      chunk: int = 64) -> int:
+    return int(_lib().gdn_delta_rule_prefill_workspace_size(T, N, Hv, dk, dv, chunk))
+
+
+def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, o, workspace,
+                               *, chunk: int = 64, qk_l2norm: bool = False, stream=None):
+    """Chunked prefill over packed sequences. q, k [T, Hk, dk]; v [T, Hv, dv];
+    a, b [T, Hv]; cu_seqlens [N+1]; S [N, Hv, dv, dk] (initial in, final out);
+    has_initial_state uint8 [N] or None; o [T, Hv, dv]; workspace uint8 tensor
+    of at least delta_rule_prefill_workspace_size(...) bytes."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    assert k.stride(0) == q.stride(0), "q and k share one token stride"
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib().gdn_delta_rule_prefill_chunked(
+        _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
+        _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
+        chunk, int(qk_l2norm), _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "gdn_delta_rule_prefill_chunked")
+
+
+def status_string(status: int) -> str:
+    return _lib().gdn_status_string(status).decode()

@@ -1,0 +1,239 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) token-mixer hot path on GB300
+ * (sm_103a).
+ *
+ * The path has two parts, both from the Qwen3.5-style hybrid serving engine
+ * that the pages "perf(gdn): dispatch exact causal-conv chunks" and "RTX 5070
+ * Ti: close Qwen3.5-4B TTFT, TPOT, and VRAM gaps vs vLLM" optimise:
+ *   1. a varlen depthwise causal conv1d (width 4, SiLU, rolling conv_state),
+ *      dispatched over exact (sequence, 8-token chunk) descriptors that are
+ *      built once per engine step and reused by every GDN layer;
+ *   2. the gated delta rule
+ *          S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,  o_t = S_t q_t
+ *      as a single-token decode update and as a chunked (WY/UT) prefill.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument that names a tensor is a DEVICE pointer (memory of
+ *   the current CUDA device) unless its comment says "host". The caller owns
+ *   all memory; the library allocates nothing. Scratch memory is passed in
+ *   explicitly (the prefill "workspace").
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream). Every call is asynchronous on that stream: it validates its
+ *   arguments on the host, enqueues kernels and returns. No call synchronises
+ *   with the device.
+ * - BF16 is IEEE bfloat16 (stored as 16-bit patterns); arithmetic is float32
+ *   with round-to-nearest-even on every BF16 store.
+ * - Validation happens before any launch. A failed check returns a negative
+ *   gdn_status_t and enqueues nothing; outputs are then untouched. Shapes with
+ *   zero tokens or zero sequences are valid and enqueue nothing. A CUDA launch
+ *   failure returns GDN_ERR_CUDA (the CUDA error string is then available from
+ *   gdn_last_cuda_error_string()).
+ * - Vector paths need 16-byte alignment: every BF16 tensor pointer, the
+ *   float32 state pointer and the conv weights must be 16-byte aligned, and
+ *   row strides (in elements) must be multiples of 8.
+ * - Contents of device buffers (cu_seqlens values, descriptor counts) cannot be
+ *   checked on the host. Kernels that read cu_seqlens treat a decreasing or
+ *   out-of-range entry as an empty sequence; gdn_build_conv_chunks also
+ *   reports such input through its optional device status word.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+typedef enum gdn_status_t {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1, /* NULL pointer, negative size, bad stride, half-set descriptor pair */
+  GDN_ERR_UNSUPPORTED = -2, /* valid but not implemented: K != 4, head dims, channel count */
+  GDN_ERR_ALIGNMENT = -3,   /* a pointer or stride breaks the 16-byte rule */
+  GDN_ERR_WORKSPACE = -4,   /* workspace too small, or descriptor capacity exceeded */
+  GDN_ERR_CUDA = -5,        /* a CUDA call failed */
+  GDN_ERR_TIMEOUT = -6      /* reserved: a bounded device-side wait gave up */
+} gdn_status_t;
+
+/*
+ * One exact conv dispatch unit: tokens [tok_start, tok_start + len) of
+ * sequence `seq`, whose first token sits at position `pos_in_seq` of that
+ * sequence. 16 bytes, four int32 fields, no padding.
+ * Source: "perf(gdn): dispatch exact causal-conv chunks", What changed
+ * (exact (sequence, 8-token chunk) descriptors).
+ */
+typedef struct gdn_conv_chunk_t {
+  int32_t seq;
+  int32_t tok_start;
+  int32_t len;
+  int32_t pos_in_seq;
+} gdn_conv_chunk_t;
+
+/*
+ * Build the exact (sequence, chunk) descriptors of one engine step.
+ * Source: "perf(gdn): dispatch exact causal-conv chunks", What changed (built
+ * once per step, uploaded once, reused across layers) and its reviewer
+ * comment (mirrors the upstream causal-conv metadata builder).
+ *
+ *   cu_seqlens    device int32 [num_seqs + 1], packed offsets; cu[0] must be 0
+ *                 and the entries non-decreasing.
+ *   num_seqs      N >= 0.
+ *   chunk_tokens  tokens per descriptor (8 on the engine path), at least 3
+ *                 (K - 1): the conv then has exactly one descriptor per
+ *                 sequence that reads the old conv_state, which lets it update
+ *                 the state in place. Any value at least the longest sequence
+ *                 gives whole-sequence descriptors. Smaller values return
+ *                 GDN_ERR_INVALID_ARG.
+ *   chunks        device gdn_conv_chunk_t [capacity], 16-byte aligned (output).
+ *   capacity      entries available in `chunks`; sum_s ceil(L_s / chunk_tokens)
+ *                 is at most floor(T / chunk_tokens) + N.
+ *   num_chunks    device int32 [1] (output): the descriptor count.
+ *   device_status device int32 [1] or NULL (output): GDN_OK, or
+ *                 GDN_ERR_INVALID_ARG for malformed cu_seqlens, or
+ *                 GDN_ERR_WORKSPACE when the count exceeds `capacity`. In
+ *                 both error cases *num_chunks is set to 0, so conv launches
+ *                 that read it do nothing.
+ * Order: sequence-major, chunks ascending; fields as in gdn_conv_chunk_t;
+ * empty sequences emit nothing. One kernel launch, no host synchronisation.
+ */
+GDN_API gdn_status_t gdn_build_conv_chunks(const int32_t* cu_seqlens, int32_t num_seqs,
+                                   int32_t chunk_tokens, gdn_conv_chunk_t* chunks,
+                                   int32_t capacity, int32_t* num_chunks,
+                                   int32_t* device_status, void* stream);
+
+/*
+ * Varlen depthwise causal conv1d prefill (width K = 4) with SiLU and a rolling
+ * state. Source: "perf(gdn): dispatch exact causal-conv chunks", What changed
+ * (one program per descriptor; whole-sequence mapping kept as the rollback)
+ * and "RTX 5070 Ti ...", Existing evidence (the K=4 specialisation).
+ *
+ * For sequence s, channel c and local position i:
+ *   y[cu[s]+i, c] = SiLU(bias[c] + sum_{j=0..3} w[c, j] * xw(i - 3 + j)),
+ *   xw(m) = x[cu[s]+m, c] for m >= 0; conv_state[s, c, 3+m] for m < 0 when
+ *   has_initial_state[s] != 0, else 0.
+ * conv_state[s] is then replaced by the last 3 entries of (initial state ++
+ * x_s); sequences with no tokens keep their state.
+ *
+ *   x                  BF16 [T, C], row stride x_stride elements (>= C, % 8 == 0).
+ *   w                  BF16 [C, 4] contiguous.   bias  BF16 [C] or NULL (zero).
+ *   conv_state         BF16 [N, C, 3] contiguous, read and written.
+ *   has_initial_state  uint8 [N] or NULL (all zero).
+ *   cu_seqlens         int32 [N + 1].
+ *   chunks, num_chunks descriptors from gdn_build_conv_chunks (chunk_tokens
+ *                      8 on the engine path, any size >= 3), and their count; BOTH
+ *                      NULL selects whole-sequence dispatch (one program per
+ *                      sequence, byte-identical output). Exactly one NULL is
+ *                      GDN_ERR_INVALID_ARG.
+ *   max_chunks         the grid bound: the capacity used to build `chunks`
+ *                      (ignored in whole-sequence mode).
+ *   T, C, K, N         tokens, channels (% 8 == 0), taps (4 only), sequences.
+ *   silu               1 applies SiLU, 0 returns the pre-activation.
+ *   y                  BF16 [T, C] contiguous (output). Must not alias x.
+ */
+GDN_API gdn_status_t gdn_causal_conv1d_fwd(const void* x, int64_t x_stride, const void* w,
+                                   const void* bias, void* conv_state,
+                                   const uint8_t* has_initial_state,
+                                   const int32_t* cu_seqlens,
+                                   const gdn_conv_chunk_t* chunks,
+                                   const int32_t* num_chunks, int32_t max_chunks,
+                                   int32_t T, int32_t C, int32_t K, int32_t N,
+                                   int32_t silu, void* y, void* stream);
+
+/*
+ * One decode token per sequence through the conv, rolling the state.
+ * Window (conv_state[n,c,0..2], x[n,c]); y = SiLU(bias + sum_j w[c,j] win_j);
+ * conv_state[n,c] <- (conv_state[n,c,1], conv_state[n,c,2], x[n,c]).
+ *
+ *   x           BF16 [N, C], row stride x_stride (>= C, % 8 == 0).
+ *   w, bias     as for gdn_causal_conv1d_fwd.
+ *   conv_state  BF16 [N, C, 3], read and written.
+ *   y           BF16 [N, C] contiguous (output).
+ */
+GDN_API gdn_status_t gdn_causal_conv1d_update(const void* x, int64_t x_stride, const void* w,
+                                      const void* bias, void* conv_state, int32_t N,
+                                      int32_t C, int32_t K, int32_t silu, void* y,
+                                      void* stream);
+
+/*
+ * Single-token gated delta-rule update for N sequences.
+ * Source: "RTX 5070 Ti ...", Existing evidence (fused decode; the state tile
+ * held in registers across the update; vector state stores).
+ *
+ * For sequence n and v-head h with q/k-head g = h / (Hv / Hk):
+ *   S' = a S;  u = b (v - S' k);  S_new = S' + u k^T;  o = S_new q,
+ * which equals a S (I - b k k^T) + b v k^T and o = S_new q. No 1/sqrt(dk) scale.
+ * With qk_l2norm != 0, q and k are first replaced by x / sqrt(sum x^2 + 1e-6).
+ *
+ *   q, k       BF16; element (n, g, i) at n * qk_stride + g * dk + i.
+ *   v          BF16; element (n, h, i) at n * v_stride + h * dv + i.
+ *   a, b       float32 [N, Hv] contiguous.
+ *   S          float32 [N, Hv, dv, dk] contiguous (row i of S is dk-contiguous),
+ *              read and written in place.
+ *   o          BF16 [N, Hv, dv] contiguous (output).
+ *   dk, dv     each one of 16, 32, 64, 128.   Hv % Hk == 0.
+ */
+GDN_API gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stride,
+                                   const void* v, int64_t v_stride, const float* a,
+                                   const float* b, float* S, void* o, int32_t N,
+                                   int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                   int32_t qk_l2norm, void* stream);
+
+/*
+ * Bytes of device workspace that gdn_delta_rule_prefill_chunked needs for these
+ * sizes (0 for invalid sizes). Pure host arithmetic.
+ */
+GDN_API size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv,
+                                             int32_t dk, int32_t dv, int32_t chunk);
+
+/*
+ * Chunked (WY/UT) prefill of the gated delta rule over packed sequences.
+ * The recurrence is the one of gdn_delta_rule_decode applied token by token;
+ * the chunked form reaches the same result up to rounding. Chunks of `chunk`
+ * tokens start at each sequence's first token and never cross sequences; the
+ * last chunk of a sequence may be partial.
+ *
+ *   q, k, v, qk_stride, v_stride   as for decode, indexed by packed token t.
+ *   a, b        float32 [T, Hv].
+ *   cu_seqlens  int32 [N + 1].
+ *   S           float32 [N, Hv, dv, dk]: the initial state of sequence s where
+ *               has_initial_state[s] != 0 (zeros otherwise), replaced by the
+ *               final state. Sequences with no tokens keep S unchanged.
+ *   has_initial_state  uint8 [N] or NULL (all zero).
+ *   o           BF16 [T, Hv, dv] contiguous (output).
+ *   chunk       64 (the only size implemented).
+ *   workspace   device scratch of at least
+ *               gdn_delta_rule_prefill_workspace_size(T, N, Hv, dk, dv, chunk)
+ *               bytes, 256-byte aligned; contents on entry do not matter.
+ *               The call owns it until the enqueued work completes.
+ */
+GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
+                                            const void* v, int64_t v_stride,
+                                            const float* a, const float* b,
+                                            const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                            float* S, const uint8_t* has_initial_state,
+                                            void* o, int32_t Hk, int32_t Hv, int32_t dk,
+                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/* Static description of a status code (never NULL). */
+GDN_API const char* gdn_status_string(gdn_status_t status);
+
+/* Text of the CUDA error behind the most recent GDN_ERR_CUDA in this process
+ * ("" if none). The pointer stays valid until the next failing call. */
+GDN_API const char* gdn_last_cuda_error_string(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* GDN_GB300_H */

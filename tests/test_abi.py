@@ -1,0 +1,137 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch.
+
+No test here reaches a kernel launch: every call either fails validation or
+has nothing to do, so these run without a GPU. Fake pointer values are never
+dereferenced on those paths.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_linear_build_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE = 0, -1, -2, -3, -4
+A16 = 0x10000          # a 16-byte-aligned fake device address
+A8 = 0x10008           # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build_library()
+    from gated_deltanet_linear_build_gb300 import gdn
+    return gdn.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for name in ("gdn_build_conv_chunks", "gdn_causal_conv1d_fwd", "gdn_causal_conv1d_update",
+                 "gdn_delta_rule_decode", "gdn_delta_rule_prefill_chunked"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from gated_deltanet_linear_build_gb300 import gdn
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert sorted(gdn.EXPORTED_SYMBOLS) == declared_symbols()
+
+
+def test_status_strings(lib):
+    for s in (OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE, -5, -6):
+        assert lib.gdn_status_string(s).startswith(b"GDN")
+    assert lib.gdn_last_cuda_error_string() is not None
+
+
+def test_build_chunks_validation(lib):
+    f = lib.gdn_build_conv_chunks
+    assert f(None, 2, 8, A16, 10, A16, None, None) == INVALID        # no cu_seqlens
+    assert f(A16, -1, 8, A16, 10, A16, None, None) == INVALID        # negative N
+    assert f(A16, 2, 2, A16, 10, A16, None, None) == INVALID         # chunk < K - 1
+    assert f(A16, 2, 8, None, 10, A16, None, None) == INVALID        # capacity but no array
+    assert f(A16, 2, 8, A16, 10, None, None, None) == INVALID        # no count output
+    assert f(A16, 2, 8, A8, 10, A16, None, None) == ALIGN
+
+
+def conv_fwd(lib, **kw):
+    args = dict(x=A16, x_stride=64, w=A16, bias=None, state=A16, has=None, cu=A16, chunks=None,
+                num=None, max_chunks=0, T=18, C=64, K=4, N=2, silu=1, y=A16)
+    args.update(kw)
+    return lib.gdn_causal_conv1d_fwd(*args.values(), None)
+
+
+def test_conv_fwd_validation(lib):
+    assert conv_fwd(lib, chunks=A16) == INVALID                 # half-set descriptor pair
+    assert conv_fwd(lib, num=A16) == INVALID
+    assert conv_fwd(lib, x=None) == INVALID
+    assert conv_fwd(lib, cu=None) == INVALID
+    assert conv_fwd(lib, T=-1) == INVALID
+    assert conv_fwd(lib, x_stride=32) == INVALID                # stride < C
+    assert conv_fwd(lib, silu=2) == INVALID
+    assert conv_fwd(lib, K=3) == UNSUPPORTED
+    assert conv_fwd(lib, C=60, x_stride=64) == UNSUPPORTED      # C % 8
+    assert conv_fwd(lib, x_stride=68) == ALIGN
+    assert conv_fwd(lib, x=A8) == ALIGN
+    assert conv_fwd(lib, bias=A8) == ALIGN
+    assert conv_fwd(lib, chunks=A8, num=A16, max_chunks=4) == ALIGN
+    assert conv_fwd(lib, T=0) == OK                             # nothing to do
+    assert conv_fwd(lib, N=0) == OK
+
+
+def test_conv_update_validation(lib):
+    f = lib.gdn_causal_conv1d_update
+    assert f(A16, 64, A16, None, A16, 2, 64, 4, 1, None, None) == INVALID
+    assert f(A16, 64, A16, None, A16, 2, 64, 5, 1, A16, None) == UNSUPPORTED
+    assert f(A16, 64, A16, None, A8, 2, 64, 4, 1, A16, None) == ALIGN
+    assert f(A16, 64, A16, None, A16, 0, 64, 4, 1, A16, None) == OK
+
+
+def decode(lib, **kw):
+    args = dict(q=A16, k=A16, qk_stride=4096, v=A16, v_stride=4096, a=A16, b=A16, S=A16, o=A16,
+                N=32, Hk=16, Hv=32, dk=128, dv=128, l2=0)
+    args.update(kw)
+    return lib.gdn_delta_rule_decode(*args.values(), None)
+
+
+def test_decode_validation(lib):
+    assert decode(lib, S=None) == INVALID
+    assert decode(lib, Hk=12) == INVALID                        # Hv % Hk
+    assert decode(lib, qk_stride=1024) == INVALID               # stride < Hk * dk
+    assert decode(lib, l2=3) == INVALID
+    assert decode(lib, dk=96) == UNSUPPORTED
+    assert decode(lib, dv=256, v_stride=8192) == UNSUPPORTED
+    assert decode(lib, qk_stride=4100) == ALIGN
+    assert decode(lib, S=A8) == ALIGN
+    assert decode(lib, N=0) == OK
+
+
+def prefill(lib, **kw):
+    args = dict(q=A16, k=A16, qk_stride=4096, v=A16, v_stride=4096, a=A16, b=A16, cu=A16, N=2,
+                T=2048, S=A16, has=None, o=A16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, l2=0,
+                ws=A16 * 16, ws_bytes=1 << 40)
+    args.update(kw)
+    return lib.gdn_delta_rule_prefill_chunked(*args.values(), None)
+
+
+def test_prefill_validation(lib):
+    need = lib.gdn_delta_rule_prefill_workspace_size(2048, 2, 32, 128, 128, 64)
+    assert need > 0
+    assert lib.gdn_delta_rule_prefill_workspace_size(2048, 2, 32, 128, 128, 32) == 0
+    assert prefill(lib, cu=None) == INVALID
+    assert prefill(lib, chunk=32) == UNSUPPORTED
+    assert prefill(lib, dk=64) == UNSUPPORTED                   # dk != dv
+    assert prefill(lib, ws_bytes=need - 1) == WORKSPACE
+    assert prefill(lib, ws=None) == WORKSPACE
+    assert prefill(lib, ws=A16 * 16 + 16) == ALIGN              # workspace 256-byte rule
+    assert prefill(lib, T=0) == OK
+    assert prefill(lib, N=0) == OK
