@@ -1,0 +1,618 @@
+"""Throughput of the GDN token-mixer hot path on the serving-mix sweep.
+
+Workload (one "step" of this benchmark = one full sweep): 24 GDN layers of the
+Qwen3.5-4B shape (conv over 8192 channels = q 16x128 | k 16x128 | v 32x128,
+width 4, SiLU; delta rule with 32 v-heads over 16 q/k-heads, d = 128), 32
+sequences with prompt lengths U[512, 1024] (seed 4) packed in order into
+prefill steps of at most 2048 tokens, then 128 decode steps over all 32
+sequences. Every prefill step builds its exact 8-token conv descriptors once
+and reuses them in all 24 layers; each layer runs the conv (prefill or update)
+and the delta rule (chunked prefill or decode) on q/k/v read in place from the
+conv output, q/k L2-normalised in the kernel. Inputs are synthetic (seeded
+normal x, gates a = exp(-softplus(z)), b = sigmoid(z)) and distinct for every
+layer and step (about 11 GB per sweep, far larger than L2).
+
+The sweep is captured once as a CUDA graph and replayed; `value` is tokens
+through the 24-layer stack per second with inputs resident in HBM. `e2e` runs
+the same sweep with every layer input copied from pinned host memory and every
+layer output copied back inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+LAYERS = 24
+N_SEQS = 32
+STEP_TOKENS = 2048
+DECODE_STEPS = 128
+HK, HV, D = 16, 32, 128
+C = 2 * HK * D + HV * D
+CHUNK = 64
+METRIC = "GDN tokens/s per step mix (prefill+decode) and achieved HBM GB/s / % roofline"
+WORKLOAD = ("serving-mix sweep: 24 GDN layers (conv 8192 ch K=4 + gated delta rule 32v/16k "
+            "heads d=128), 32 seqs, prompts U[512,1024] seed 4 packed into 2048-token prefill "
+            "steps, then 128 decode steps")
+KINDS = ("build_chunks", "conv_prefill", "delta_prefill", "conv_update", "delta_decode")
+KERNEL_SOURCES = {
+    "build_chunks": "gated_deltanet_linear_build_gb300/csrc/conv.cu",
+    "conv_prefill": "gated_deltanet_linear_build_gb300/csrc/conv.cu",
+    "conv_update": "gated_deltanet_linear_build_gb300/csrc/conv.cu",
+    "delta_decode": "gated_deltanet_linear_build_gb300/csrc/decode.cu",
+    "delta_prefill": "gated_deltanet_linear_build_gb300/csrc/prefill.cu",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# Multi-rank plumbing (weak scaling: every rank runs its own independent mix)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_over_ranks(x: float, op: str, dist=None, device="cpu") -> float:
+    """MAX or SUM of a per-rank scalar (identity on one rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_lengths_seed(rank: int) -> int:
+    """Rank 0 serves the seed-4 prompt mix; rank r its own mix (seed 4 + r)."""
+    return 4 + rank
+
+
+# ----------------------------------------------------------------------------
+# Peaks, clocks, stored ncu traffic
+# ----------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return (float(pk["hbm_gbs"]), float(pk["bf16_tflops"]),
+                float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), "measured")
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def source_digest(relpath: str) -> str:
+    with open(os.path.join(ROOT, relpath), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def stored_traffic(kind: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed after the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kind]
+        if source_digest(rec["source"]) != rec["source_sha256_16"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            t_end = time.time() + 5.0          # let sampling start before timing
+            while not self.lines and time.time() < t_end and self.proc.poll() is None:
+                time.sleep(0.02)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                mhz.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------------------
+# Algorithmic work per launch (bytes / flops), for the rooflines
+# ----------------------------------------------------------------------------
+
+def decode_delta_bytes(n=N_SEQS):
+    state = 2 * n * HV * D * D * 4                 # S read + write (float32)
+    qkv = n * (2 * HK * D + HV * D) * 2            # q, k, v (BF16)
+    gates = 2 * n * HV * 4
+    out = n * HV * D * 2
+    return state + qkv + gates + out
+
+
+def conv_prefill_bytes(T, n_seqs):
+    return 2 * T * C * 2 + C * 4 * 2 + 2 * n_seqs * C * 3 * 2
+
+
+def conv_update_bytes(n=N_SEQS):
+    return 2 * n * C * 2 + 2 * n * C * 3 * 2 + C * 4 * 2
+
+
+def prefill_flops(chunk_lengths, d=D, hv=HV):
+    """Algorithmic flops of the chunked prefill over chunks of the given sizes,
+    all v-heads: K K^T, Q K^T, Tm K, Tm V and (M o QK^T) Delta at c^2 d MACs;
+    W S^T, Q S^T and Delta^T K at c d^2 MACs; forward substitution c^3 / 6."""
+    macs = 0.0
+    for c in chunk_lengths:
+        macs += 5 * c * c * d + 3 * c * d * d + c ** 3 / 6
+    return 2.0 * macs * hv
+
+
+def prefill_bytes(T, n_seqs):
+    per_tok = 2 * HK * D * 2 + HV * D * 2 + 2 * HV * 4 + HV * D * 2   # q,k,v,a,b,o
+    return T * per_tok + 2 * n_seqs * HV * D * D * 4                  # + S in/out
+
+
+# ----------------------------------------------------------------------------
+# The workload on the device
+# ----------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, rank: int, device):
+        import torch
+        from gated_deltanet_linear_build_gb300 import stack as stk, synth
+        self.torch = torch
+        self.lengths = [int(x) for x in synth.serving_mix_lengths(rank_lengths_seed(rank))]
+        self.steps = stk.pack_prefill_steps(self.lengths, STEP_TOKENS)
+        seed = 1000 + rank
+        self.stack = stk.GdnLayerStack(LAYERS, N_SEQS, hk=HK, hv=HV, d=D,
+                                       max_step_tokens=STEP_TOKENS, device=device, seed=seed)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed + 1)
+        self.meta = []
+        for st in self.steps:
+            cu, has, first = self.stack.step_meta(st)
+            self.meta.append((torch.tensor(cu, dtype=torch.int32, device=device),
+                              torch.tensor(has, dtype=torch.uint8, device=device), first,
+                              len(has), int(st.tokens)))
+        bf16 = torch.bfloat16
+
+        def gates(T):
+            z1 = torch.randn((T, HV), generator=g, device=device)
+            z2 = torch.randn((T, HV), generator=g, device=device)
+            return (torch.exp(-torch.nn.functional.softplus(z1)).contiguous(),
+                    torch.sigmoid(z2).contiguous())
+
+        self.px = [[torch.randn((m[4], C), generator=g, device=device, dtype=bf16)
+                    for _ in range(LAYERS)] for m in self.meta]
+        self.pg = [[gates(m[4]) for _ in range(LAYERS)] for m in self.meta]
+        self.dx = [[torch.randn((N_SEQS, C), generator=g, device=device, dtype=bf16)
+                    for _ in range(LAYERS)] for _ in range(DECODE_STEPS)]
+        self.dg = [[gates(N_SEQS) for _ in range(LAYERS)] for _ in range(DECODE_STEPS)]
+        self.py = [torch.empty((STEP_TOKENS, C), dtype=bf16, device=device) for _ in range(LAYERS)]
+        self.po = [torch.empty((STEP_TOKENS, HV, D), dtype=bf16, device=device)
+                   for _ in range(LAYERS)]
+        self.dy = [torch.empty((N_SEQS, C), dtype=bf16, device=device) for _ in range(LAYERS)]
+        self.do = [torch.empty((N_SEQS, HV, D), dtype=bf16, device=device) for _ in range(LAYERS)]
+        self.prefill_tokens = sum(self.lengths)
+        self.decode_tokens = DECODE_STEPS * N_SEQS
+        self.tokens = self.prefill_tokens + self.decode_tokens
+
+    def chunk_lengths(self):
+        return [min(CHUNK, s.length - CHUNK * j) for st in self.steps for s in st.segments
+                for j in range(-(-s.length // CHUNK))]
+
+    def sweep(self, timer=None):
+        """Enqueue one full sweep (all prefill steps, then all decode steps)."""
+        for i, (cu, has, first, n, T) in enumerate(self.meta):
+            ys = [y[:T] for y in self.py]
+            os_ = [o[:T] for o in self.po]
+            self.stack.prefill_step(cu, has, first, n, self.px[i], self.pg[i], ys, os_,
+                                    timer=timer)
+        for j in range(DECODE_STEPS):
+            self.stack.decode_step(self.dx[j], self.dg[j], self.dy, self.do, timer=timer)
+
+
+class E2EWorkload:
+    """The same sweep fed from pinned host memory: every layer input (x, a, b,
+    and the step's cu_seqlens / flags) is copied host->device before its layer
+    and every layer output o is copied device->host after it."""
+
+    def __init__(self, wl: Workload):
+        torch = wl.torch
+        self.wl = wl
+        pin = dict(pin_memory=True)
+        self.hpx = [torch.randn((STEP_TOKENS, C), dtype=torch.bfloat16).pin_memory()
+                    for _ in range(LAYERS)]
+        self.hpa = [torch.rand((STEP_TOKENS, HV), **pin) for _ in range(LAYERS)]
+        self.hpb = [torch.rand((STEP_TOKENS, HV), **pin) for _ in range(LAYERS)]
+        self.hdx = [torch.randn((N_SEQS, C), dtype=torch.bfloat16).pin_memory()
+                    for _ in range(LAYERS)]
+        self.hda = [torch.rand((N_SEQS, HV), **pin) for _ in range(LAYERS)]
+        self.hdb = [torch.rand((N_SEQS, HV), **pin) for _ in range(LAYERS)]
+        self.hpo = [torch.empty((STEP_TOKENS, HV, D), dtype=torch.bfloat16, **pin)
+                    for _ in range(LAYERS)]
+        self.hdo = [torch.empty((N_SEQS, HV, D), dtype=torch.bfloat16, **pin)
+                    for _ in range(LAYERS)]
+        self.hcu = [m[0].cpu().pin_memory() for m in wl.meta]
+        self.hhas = [m[1].cpu().pin_memory() for m in wl.meta]
+        self.h2d = 0
+        self.d2h = 0
+
+    def sweep(self):
+        wl, st = self.wl, self.wl.stack
+        h2d = d2h = 0
+        for i, (cu, has, first, n, T) in enumerate(wl.meta):
+            cu.copy_(self.hcu[i], non_blocking=True)
+            has.copy_(self.hhas[i], non_blocking=True)
+            h2d += cu.numel() * 4 + has.numel()
+            xs, gs = wl.px[i], wl.pg[i]
+            for l in range(LAYERS):
+                xs[l].copy_(self.hpx[l][:T], non_blocking=True)
+                gs[l][0].copy_(self.hpa[l][:T], non_blocking=True)
+                gs[l][1].copy_(self.hpb[l][:T], non_blocking=True)
+                h2d += T * C * 2 + 2 * T * HV * 4
+            ys = [y[:T] for y in wl.py]
+            os_ = [o[:T] for o in wl.po]
+            st.prefill_step(cu, has, first, n, xs, gs, ys, os_)
+            for l in range(LAYERS):
+                self.hpo[l][:T].copy_(os_[l], non_blocking=True)
+                d2h += T * HV * D * 2
+        for j in range(DECODE_STEPS):
+            xs, gs = wl.dx[j], wl.dg[j]
+            for l in range(LAYERS):
+                xs[l].copy_(self.hdx[l], non_blocking=True)
+                gs[l][0].copy_(self.hda[l], non_blocking=True)
+                gs[l][1].copy_(self.hdb[l], non_blocking=True)
+                h2d += N_SEQS * C * 2 + 2 * N_SEQS * HV * 4
+            st.decode_step(xs, gs, wl.dy, wl.do)
+            for l in range(LAYERS):
+                self.hdo[l].copy_(wl.do[l], non_blocking=True)
+                d2h += N_SEQS * HV * D * 2
+        self.h2d, self.d2h = h2d, d2h
+
+
+class EventTimer:
+    """Timing events around every library call, recorded as event nodes of
+    the captured graph (so each replay re-records them on the launch stream)."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.ev = {k: ([], []) for k in KINDS}
+
+    def __call__(self, kind, edge):
+        e = self.torch.cuda.Event(enable_timing=True, external=True)
+        e.record(self.torch.cuda.current_stream())
+        self.ev[kind][0 if edge == "start" else 1].append(e)
+
+    def durations_ms(self, kind):
+        s, e = self.ev[kind]
+        return [a.elapsed_time(b) for a, b in zip(s, e)]
+
+
+def events_supported(torch) -> bool:
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+# ----------------------------------------------------------------------------
+
+CPU_SAMPLE = ("oracle (float64 numpy, 1 thread) on one layer: a 32-sequence decode step "
+              "(conv update + delta decode) and a 2x128-token prefill slice (conv + sequential "
+              "delta rule, 32 heads); per-token-layer times scaled to the 24-layer mix")
+
+
+def cpu_oracle_sample(seconds: float):
+    """Oracle seconds per token-layer for decode and for prefill, on a sample
+    of one layer of the mix (see CPU_SAMPLE); repeats until `seconds` spent."""
+    from oracle import gdn_oracle as O
+    from gated_deltanet_linear_build_gb300 import synth
+
+    conv_d = synth.conv_update_case(11, N_SEQS, C)
+    dd = synth.delta_case(12, [1] * N_SEQS, HK, HV, D, D, s0_std=0.02, normed_qk=False)
+    conv_p = synth.conv_case(13, [128, 128], C, initial_state=False)
+    dp = synth.delta_case(14, [128, 128], HK, HV, D, D, normed_qk=False)
+    t_dec = t_pre = 0.0
+    n_dec = n_pre = 0
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end or n_dec == 0:
+        t0 = time.perf_counter()
+        O.causal_conv1d_update(conv_d["x"], conv_d["w"], None, conv_d["conv_state"])
+        O.delta_rule_decode(dd["q"], dd["k"], dd["v"], dd["a"], dd["b"], dd["S0"], qk_l2norm=True)
+        t1 = time.perf_counter()
+        O.causal_conv1d_fwd(conv_p["x"], conv_p["w"], None, conv_p["conv_state"],
+                            conv_p["has_initial_state"], conv_p["cu_seqlens"])
+        O.delta_rule_prefill(dp["q"], dp["k"], dp["v"], dp["a"], dp["b"], dp["cu_seqlens"],
+                             dp["S0"], dp["has_initial_state"], qk_l2norm=True)
+        t2 = time.perf_counter()
+        t_dec += t1 - t0
+        t_pre += t2 - t1
+        n_dec += N_SEQS
+        n_pre += 256
+    return t_dec / n_dec, t_pre / n_pre, t_dec + t_pre
+
+
+def mix_tokens_per_s(per_dec, per_pre, prefill_tokens, decode_tokens):
+    t = LAYERS * (prefill_tokens * per_pre + decode_tokens * per_dec)
+    return (prefill_tokens + decode_tokens) / t
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    from gated_deltanet_linear_build_gb300 import synth
+    pre = int(sum(int(x) for x in synth.serving_mix_lengths(rank_lengths_seed(0))))
+    dec = DECODE_STEPS * N_SEQS
+    per_step = max(1.0, min(args.cpu_seconds, 20.0))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(0.0)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        pd, pp, _ = cpu_oracle_sample(per_step / 2)
+        secs.append(time.perf_counter() - t0)
+        vals.append(mix_tokens_per_s(pd, pp, pre, dec))
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": CPU_SAMPLE},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": CPU_SAMPLE},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# The GPU arm
+# ----------------------------------------------------------------------------
+
+def kernel_report(wl, timer, hbm_peak, bf16_peak):
+    """Per kind: launches, average duration, share of the sweep, and achieved
+    rate against its roofline (algorithmic work / average duration)."""
+    rep = {}
+    total = 0.0
+    durs = {k: timer.durations_ms(k) for k in KINDS}
+    for k in KINDS:
+        total += sum(durs[k])
+    n_steps = len(wl.steps)
+    chunk_fl = prefill_flops(wl.chunk_lengths()) / n_steps
+    work = {
+        "delta_decode": ("hbm", decode_delta_bytes()),
+        "conv_update": ("hbm", conv_update_bytes()),
+        "conv_prefill": ("hbm", sum(conv_prefill_bytes(st.tokens, len(st.segments))
+                                    for st in wl.steps) / n_steps),
+        "delta_prefill": ("tensor", chunk_fl),
+    }
+    for k in KINDS:
+        if not durs[k]:
+            continue
+        avg = statistics.mean(durs[k])
+        r = {"launches": len(durs[k]), "avg_us": avg * 1e3,
+             "share": sum(durs[k]) / total if total else None}
+        if k in work:
+            bound, amount = work[k]
+            if bound == "hbm":
+                ach = amount / (avg / 1e3) / 1e9
+                r.update(bound="hbm", achieved=ach, unit="GB/s", peak=hbm_peak,
+                         frac=ach / hbm_peak, algorithmic_per_launch=amount)
+            else:
+                ach = amount / (avg / 1e3) / 1e12
+                r.update(bound="tensor", achieved=ach, unit="TFLOP/s", peak=bf16_peak,
+                         frac=ach / bf16_peak, algorithmic_per_launch=amount)
+        rep[k] = r
+    return rep
+
+
+def run_gdn(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    from gated_deltanet_linear_build_gb300 import build as B
+    B.build_library()
+    from gated_deltanet_linear_build_gb300 import gdn
+    gdn.load_library()
+
+    hbm_peak, bf16_peak, _bf16_sus, peak_src = load_peaks()
+    wl = Workload(rank, dev)
+    stream = torch.cuda.Stream(device=dev)
+    timer = EventTimer(torch) if events_supported(torch) else None
+
+    with torch.cuda.stream(stream):
+        wl.sweep()                      # eager warm run (sets kernel attributes)
+    torch.cuda.synchronize()
+    launches_before = wl.stack.launches
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        wl.sweep(timer)
+    launches_per_sweep = wl.stack.launches - launches_before
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms = start.elapsed_time(end) / args.steps
+    ms_max = reduce_over_ranks(ms, "max", dist, dev)
+    tokens_all = reduce_over_ranks(float(wl.tokens), "sum", dist, dev)
+    value = tokens_all / (ms_max / 1e3)
+
+    kernels = kernel_report(wl, timer, hbm_peak, bf16_peak) if timer else {}
+    roofline = None
+    if kernels:
+        dom = max((k for k in kernels if "bound" in kernels[k]),
+                  key=lambda k: kernels[k]["share"])
+        r = kernels[dom]
+        roofline = {"kernel": dom, "bound": r["bound"], "achieved": r["achieved"],
+                    "peak": r["peak"], "unit": r["unit"], "frac": r["frac"],
+                    "peak_source": peak_src, "share_of_sweep": r["share"],
+                    "avg_launch_us": r["avg_us"], "launches_timed": r["launches"],
+                    "algorithmic_per_launch": r["algorithmic_per_launch"],
+                    "traffic": stored_traffic(dom)}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "layers": LAYERS, "seqs_per_gpu": N_SEQS,
+                   "prefill_tokens": wl.prefill_tokens, "decode_tokens": wl.decode_tokens,
+                   "prefill_steps": len(wl.steps), "step_tokens": STEP_TOKENS,
+                   "conv_channels": C, "v_heads": HV, "qk_heads": HK, "head_dim": D,
+                   "l2": "inputs larger than L2 (about 11 GB of distinct layer inputs per sweep)",
+                   "timing": "CUDA graph of one sweep, replayed; CUDA events on its stream; "
+                             "per-kernel times from event nodes of the last replay",
+                   "parallelism": f"dp{world} (independent sequences per GPU)"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": launches_per_sweep * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+    if not args.no_e2e:
+        e2 = E2EWorkload(wl)
+        with torch.cuda.stream(stream):
+            e2.sweep()
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            e2.sweep()
+        for _ in range(max(1, args.warmup)):
+            g2.replay()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        s2, e2_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            g2.replay()
+        e2_.record(stream)
+        torch.cuda.synchronize()
+        ms2 = reduce_over_ranks(s2.elapsed_time(e2_) / args.steps, "max", dist, dev)
+        out["e2e"] = {"value": tokens_all / (ms2 / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": e2.h2d, "d2h_bytes_per_step": e2.d2h,
+                      "ms_per_step": ms2,
+                      "path": "C-ABI calls on buffers copied from/to pinned host memory "
+                              "every layer (cudaMemcpyAsync), inside the graph"}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        pd, pp, spent = cpu_oracle_sample(args.cpu_seconds)
+        out["cpu_baseline"] = {
+            "value": mix_tokens_per_s(pd, pp, wl.prefill_tokens, wl.decode_tokens),
+            "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": CPU_SAMPLE,
+            "cpu_seconds": spent}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gdn(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -287,13 +287,22 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   if (rc != GDN_OK) return rc;
 
   constexpr int PK = DK + 1, PV = DV + 1, PT = kChunk + 1, PS = SL + 1;
-  const size_t smem1 = sizeof(float) * (kChunk * PK + kChunk * PV + 2 * kChunk * PT + 3 * kChunk);
-  const size_t smem2 = sizeof(float) * (SL * PK + 3 * kChunk * PK + 2 * kChunk * PS +
-                                        kChunk * PT + kChunk);
+  constexpr size_t smem1 =
+      sizeof(float) * (kChunk * PK + kChunk * PV + 2 * kChunk * PT + 3 * kChunk);
+  constexpr size_t smem2 =
+      sizeof(float) * (SL * PK + 3 * kChunk * PK + 2 * kChunk * PS + kChunk * PT + kChunk);
   auto k1 = intra_chunk_kernel<DK, DV>;
   auto k2 = state_pass_kernel<DK, DV, SL>;
-  cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-  cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+  // Opt in to more than 48 KB of dynamic shared memory, once per process (not a
+  // stream operation, so it is also safe while a stream is being captured).
+  static const bool smem_attrs = [] {
+    cudaFuncSetAttribute(intra_chunk_kernel<DK, DV>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    cudaFuncSetAttribute(state_pass_kernel<DK, DV, SL>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
+    return true;
+  }();
+  (void)smem_attrs;
   k1<<<dim3(L.capacity, Hv), kThreads, smem1, st>>>(kp, qk_stride, vp, v_stride, a, b, count,
                                                      desc, T, Hk, Hv, l2, g_ws, w_ws, u_ws);
   if ((rc = check_launch()) != GDN_OK) return rc;

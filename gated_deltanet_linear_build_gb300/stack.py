@@ -26,6 +26,9 @@ import torch
 
 from . import gdn
 
+# Kernels enqueued by one gdn_delta_rule_prefill_chunked call.
+PREFILL_LAUNCHES = 3
+
 
 @dataclass
 class Segment:
@@ -121,39 +124,44 @@ class GdnLayerStack:
         return cu, has, slots[0]
 
     def prefill_step(self, cu_d, has_d, first_slot: int, n: int, xs, gates, ys, outs,
-                     layer_hook=None):
+                     timer=None):
         """One prefill engine step over all layers.
 
         cu_d: int32 [n+1] on the device; has_d: uint8 [n]; xs[l]: BF16 [T, C]
         inputs; gates[l]: (a, b) float32 [T, Hv]; ys[l]: BF16 [T, C] conv
-        outputs; outs[l]: BF16 [T, Hv, d] delta outputs.
+        outputs; outs[l]: BF16 [T, Hv, d] delta outputs. ``timer(kind, edge)``,
+        if given, is called before ("start") and after ("end") every call.
         """
+        tick = timer if timer is not None else (lambda kind, edge: None)
+        tick("build_chunks", "start")
         gdn.build_conv_chunks(cu_d, self.chunks, self.num_chunks, chunk_tokens=8)
+        tick("build_chunks", "end")
         self.launches += 1
         sl = slice(first_slot, first_slot + n)
         for l in range(self.layers):
             x, y = xs[l], ys[l]
+            tick("conv_prefill", "start")
             gdn.causal_conv1d_fwd(x, self.w[l], None, self.conv_state[l][sl], has_d, cu_d, y,
                                   chunks=self.chunks, num_chunks=self.num_chunks)
+            tick("conv_prefill", "end")
             q, k, v = self.qkv(y)
             a, b = gates[l]
-            if layer_hook is not None:
-                layer_hook("prefill_start", l)
+            tick("delta_prefill", "start")
             gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, outs[l],
                                            self.workspace, qk_l2norm=True)
-            if layer_hook is not None:
-                layer_hook("prefill_end", l)
-            self.launches += 4
+            tick("delta_prefill", "end")
+            self.launches += 1 + PREFILL_LAUNCHES
 
-    def decode_step(self, xs, gates, ys, outs, layer_hook=None):
+    def decode_step(self, xs, gates, ys, outs, timer=None):
         """One decode engine step (one token for every slot) over all layers."""
+        tick = timer if timer is not None else (lambda kind, edge: None)
         for l in range(self.layers):
+            tick("conv_update", "start")
             gdn.causal_conv1d_update(xs[l], self.w[l], None, self.conv_state[l], ys[l])
+            tick("conv_update", "end")
             q, k, v = self.qkv(ys[l])
             a, b = gates[l]
-            if layer_hook is not None:
-                layer_hook("decode_start", l)
+            tick("delta_decode", "start")
             gdn.delta_rule_decode(q, k, v, a, b, self.S[l], outs[l], qk_l2norm=True)
-            if layer_hook is not None:
-                layer_hook("decode_end", l)
+            tick("delta_decode", "end")
             self.launches += 2

@@ -184,3 +184,19 @@ def decode(seed: int = 2):
 def prefill(seed: int = 3):
     """2 x 1024 tokens, 32 v-heads over 16 k-heads, d = 128, S0 = 0."""
     return delta_case(seed, [1024, 1024], QK_HEADS, V_HEADS, HEAD_DIM, HEAD_DIM)
+
+
+# ----------------------------------------------------------------------------
+# Serving mix
+# ----------------------------------------------------------------------------
+
+SERVING_LAYERS = 24
+SERVING_SEQS = 32
+SERVING_STEP_TOKENS = 2048
+SERVING_DECODE_STEPS = 128
+
+
+def serving_mix_lengths(seed: int = 4, n: int = SERVING_SEQS, lo: int = 512, hi: int = 1024):
+    """Prompt lengths of the serving mix: n integers uniform on [lo, hi]."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, size=n).astype(np.int64)
