@@ -95,4 +95,12 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
                                   int32_t qk_l2norm, void* workspace, cudaStream_t st);
 
+// Tensor-core (tcgen05) chunked prefill for dk = dv = 128.
+size_t prefill_tc_workspace_bytes(int32_t T, int32_t N, int32_t Hv);
+gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, const void* v,
+                               int64_t v_stride, const float* a, const float* b,
+                               const int32_t* cu, int32_t N, int32_t T, float* S,
+                               const uint8_t* has_init, void* o, int32_t Hk, int32_t Hv,
+                               int32_t qk_l2norm, void* workspace, cudaStream_t st);
+
 }  // namespace gdn

@@ -20,7 +20,8 @@
 //   3. state pass, one CTA per (sequence, v-head, 32-row slice of S): walks the
 //      chunks in order, forms Delta, the outputs and the next state. Rows of S
 //      (dv index) evolve independently, so slices need no exchange.
-// All arithmetic is float32 on CUDA cores in this version.
+// This file holds the float32 CUDA-core version, used for head dims 16, 32
+// and 64; head dim 128 runs on the tensor cores (prefill_tc.cu).
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -317,6 +318,7 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
 size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                                int32_t chunk) {
   if (T < 0 || N < 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk != kChunk) return 0;
+  if (dk == 128 && dv == 128) return prefill_tc_workspace_bytes(T, N, Hv);
   return ws_layout(T, N, Hv, dk, dv).total;
 }
 
@@ -332,7 +334,7 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
     case 16: return launch_prefill_t<16>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
     case 32: return launch_prefill_t<32>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
     case 64: return launch_prefill_t<64>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
-    case 128: return launch_prefill_t<128>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
+    case 128: return launch_prefill_tc(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
   }
   return GDN_ERR_UNSUPPORTED;
 }

@@ -327,3 +327,29 @@ def test_prefill_then_decode_equals_longer_prefill(G):
         ref = bf16_values(o_full)[rows]
         assert O.rel_err(bf16_values(o_t), ref) < TOL_BF16
     assert O.rel_err(S.cpu().numpy(), S_full.cpu().numpy()) < TOL_STATE
+
+
+def test_prefill_slow_decay_state_precision(G):
+    # Gates close to 1 (a = exp(-softplus(z - 4.5))): the state keeps a long
+    # memory, so every float32 product that feeds it must keep its precision.
+    d = synth.delta_case(54, [300, 1024], 16, 32, 128, 128, s0_std=0.05)
+    rng = np.random.default_rng(55)
+    z = rng.standard_normal(d["a"].shape) - 4.5
+    d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
+    o, S = prefill_gpu(G, d)
+    check_prefill(d, o, S, heads=[0, 9, 31])
+
+
+def test_prefill_full_size_all_heads_one_sequence(G):
+    d = synth.prefill(3)
+    o, S = prefill_gpu(G, d)
+    one = {k: d[k] for k in d}
+    for key in ("q", "k", "v", "a", "b"):
+        one[key] = d[key][:1024]
+    one["cu_seqlens"] = d["cu_seqlens"][:2]
+    one["S0"] = d["S0"][:1]
+    one["has_initial_state"] = d["has_initial_state"][:1]
+    orf, Sr = O.delta_rule_prefill(one["q"], one["k"], one["v"], one["a"], one["b"],
+                                   one["cu_seqlens"], one["S0"], one["has_initial_state"])
+    assert O.rel_err(bf16_values(o)[:1024], orf) < TOL_BF16
+    assert O.rel_err(S.cpu().numpy()[:1], Sr) < TOL_STATE
