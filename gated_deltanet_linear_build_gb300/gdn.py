@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "gdn_delta_rule_decode",
     "gdn_delta_rule_prefill_workspace_size",
     "gdn_delta_rule_prefill_chunked",
+    "gdn_delta_rule_prefill_chunked_noalloc",
     "gdn_status_string",
     "gdn_last_cuda_error_string",
 )
@@ -63,6 +64,9 @@ _SIGNATURES = {
     "gdn_delta_rule_prefill_chunked": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _I32,
                                                       _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
                                                       _I32, _I32, _P, ctypes.c_size_t, _P]),
+    "gdn_delta_rule_prefill_chunked_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P,
+                                                              _I32, _I32, _P, _P, _P, _I32, _I32,
+                                                              _I32, _I32, _I32, _I32, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_cuda_error_string": (ctypes.c_char_p, []),
 }
@@ -182,6 +186,23 @@ def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, 
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
         chunk, int(qk_l2norm), _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked")
+
+
+def delta_rule_prefill_chunked_noalloc(q, k, v, a, b, cu_seqlens, S, has_initial_state, o, *,
+                                       chunk: int = 64, qk_l2norm: bool = False, stream=None):
+    """The chunked prefill without a workspace argument, for callers that may
+    not allocate device memory: scratch is the library's fixed 64 MiB device
+    array. Same arguments and results as delta_rule_prefill_chunked. Calls
+    that overlap on the GPU share that array and must be serialised."""
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    assert k.stride(0) == q.stride(0), "q and k share one token stride"
+    rc = _lib().gdn_delta_rule_prefill_chunked_noalloc(
+        _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
+        _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
+        chunk, int(qk_l2norm), _stream(stream))
+    _check(rc, "gdn_delta_rule_prefill_chunked_noalloc")
 
 
 def status_string(status: int) -> str:

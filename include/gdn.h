@@ -225,6 +225,41 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k
                                             void* workspace, size_t workspace_bytes,
                                             void* stream);
 
+/*
+ * The chunked prefill above, for callers that cannot allocate device memory.
+ * (The pages describe no such variant; it exists for integration only.)
+ *
+ * Who needs it: code that must not call cudaMalloc -- a plugin running inside
+ * a host framework that owns every device allocation through its own pool, or
+ * a call site where an allocation could block or synchronise the device. Such
+ * callers cannot provide the workspace that gdn_delta_rule_prefill_chunked
+ * takes, so this entry point takes none: its scratch is a fixed 64 MiB array
+ * inside the library, present on every GPU that loads the library until the
+ * process exits.
+ *
+ * Arguments, results and layouts are those of gdn_delta_rule_prefill_chunked,
+ * minus workspace / workspace_bytes. Sizes whose workspace
+ * (gdn_delta_rule_prefill_workspace_size) exceeds 64 MiB are rejected with
+ * GDN_ERR_WORKSPACE before anything is enqueued (for example, 2 x 512 tokens
+ * with 32 v-heads of width 128 fit; 2 x 1024 tokens do not).
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress and caches it; make that
+ * first call before capturing a stream. The call never allocates: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Sharing: every call on a device uses the same array, and the array keeps
+ * whatever the last call left in it (each call writes everything it reads
+ * back, and clears its own status word). Two calls whose work overlaps on the
+ * GPU -- on different streams, or from different host threads -- race on the
+ * array and corrupt each other's results: serialise them.
+ */
+GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
+    const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
+    const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
+    const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+    int32_t chunk, int32_t qk_l2norm, void* stream);
+
 /* Static description of a status code (never NULL). */
 GDN_API const char* gdn_status_string(gdn_status_t status);
 
