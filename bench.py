@@ -51,7 +51,7 @@ KERNEL_SOURCES = {
     "conv_prefill": "gated_deltanet_linear_build_gb300/csrc/conv.cu",
     "conv_update": "gated_deltanet_linear_build_gb300/csrc/conv.cu",
     "delta_decode": "gated_deltanet_linear_build_gb300/csrc/decode.cu",
-    "delta_prefill": "gated_deltanet_linear_build_gb300/csrc/prefill.cu",
+    "delta_prefill": "gated_deltanet_linear_build_gb300/csrc/prefill_tc.cu",
 }
 
 
@@ -64,6 +64,10 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--case", default="mix",
+                   choices=["mix", "conv_prefill", "conv_update", "decode", "prefill"],
+                   help="mix = the serving-mix sweep (the benchmark); the others time one "
+                        "hot-path call on its own workload shape (per-kernel studies, ncu)")
     return p.parse_args(argv)
 
 
@@ -607,10 +611,121 @@ def run_gdn(args):
     return 0
 
 
+def run_case(args):
+    """Time one hot-path call on its own workload shape, cycling through input
+    sets whose total exceeds twice the L2 size, CUDA events on the stream."""
+    import torch
+    from gated_deltanet_linear_build_gb300 import build as B, gdn
+    B.build_library()
+    gdn.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, _, peak_src = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    bf16 = torch.bfloat16
+    L2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def randn(*shape, dtype=torch.float32):
+        return torch.randn(shape, generator=g, device=dev, dtype=dtype)
+
+    def gates(T):
+        return (torch.exp(-torch.nn.functional.softplus(randn(T, HV))).contiguous(),
+                torch.sigmoid(randn(T, HV)).contiguous())
+
+    case = args.case
+    if case == "conv_prefill":
+        T, n = 2048, 2
+        cu = torch.tensor([0, 1024, 2048], dtype=torch.int32, device=dev)
+        has = torch.zeros(n, dtype=torch.uint8, device=dev)
+        chunks = torch.empty((T // 8 + n, 4), dtype=torch.int32, device=dev)
+        cnt = torch.empty(1, dtype=torch.int32, device=dev)
+        gdn.build_conv_chunks(cu, chunks, cnt, chunk_tokens=8)
+        per = conv_prefill_bytes(T, n)
+        sets = [(randn(T, C, dtype=bf16), (randn(C, 4) * 0.5).to(bf16),
+                 torch.zeros((n, C, 3), dtype=bf16, device=dev),
+                 torch.empty((T, C), dtype=bf16, device=dev))
+                for _ in range(max(2, int(2 * L2 // per) + 1))]
+
+        def call(i):
+            x, w, st, y = sets[i % len(sets)]
+            gdn.causal_conv1d_fwd(x, w, None, st, has, cu, y, chunks=chunks, num_chunks=cnt)
+        work, unit, bound = per, "GB/s", "hbm"
+    elif case == "conv_update":
+        per = conv_update_bytes()
+        sets = [(randn(N_SEQS, C, dtype=bf16), (randn(C, 4) * 0.5).to(bf16),
+                 randn(N_SEQS, C, 3, dtype=bf16), torch.empty((N_SEQS, C), dtype=bf16, device=dev))
+                for _ in range(int(2 * L2 // per) + 1)]
+
+        def call(i):
+            x, w, st, y = sets[i % len(sets)]
+            gdn.causal_conv1d_update(x, w, None, st, y)
+        work, unit, bound = per, "GB/s", "hbm"
+    elif case == "decode":
+        per = decode_delta_bytes()
+        sets = []
+        for _ in range(int(2 * L2 // per) + 1):
+            y = randn(N_SEQS, C, dtype=bf16)
+            a, b = gates(N_SEQS)
+            sets.append((y, a, b, randn(N_SEQS, HV, D, D) * 0.02,
+                         torch.empty((N_SEQS, HV, D), dtype=bf16, device=dev)))
+
+        def call(i):
+            y, a, b, S, o = sets[i % len(sets)]
+            q = y[:, :HK * D].view(N_SEQS, HK, D)
+            k = y[:, HK * D:2 * HK * D].view(N_SEQS, HK, D)
+            v = y[:, 2 * HK * D:].view(N_SEQS, HV, D)
+            gdn.delta_rule_decode(q, k, v, a, b, S, o, qk_l2norm=True)
+        work, unit, bound = per, "GB/s", "hbm"
+    else:  # prefill: 2 x 1024 tokens, 32 v-heads over 16 k-heads, d = 128
+        T, n = 2048, 2
+        cu = torch.tensor([0, 1024, 2048], dtype=torch.int32, device=dev)
+        has = torch.zeros(n, dtype=torch.uint8, device=dev)
+        ws = torch.empty(gdn.delta_rule_prefill_workspace_size(T, n, HV, D, D), dtype=torch.uint8,
+                         device=dev)
+        sets = []
+        for _ in range(2):
+            y = randn(T, C, dtype=bf16)
+            a, b = gates(T)
+            sets.append((y, a, b, torch.zeros((n, HV, D, D), device=dev),
+                         torch.empty((T, HV, D), dtype=bf16, device=dev)))
+
+        def call(i):
+            y, a, b, S, o = sets[i % len(sets)]
+            q = y[:, :HK * D].view(T, HK, D)
+            k = y[:, HK * D:2 * HK * D].view(T, HK, D)
+            v = y[:, 2 * HK * D:].view(T, HV, D)
+            gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu, S, has, o, ws, qk_l2norm=True)
+        work, unit, bound = prefill_flops([64] * 32), "TFLOP/s", "tensor"
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            call(i)
+        torch.cuda.synchronize()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        for i in range(args.steps):
+            call(i)
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+    us = s_ev.elapsed_time(e_ev) * 1e3 / args.steps
+    scale = 1e9 if unit == "GB/s" else 1e12
+    ach = work / (us / 1e6) / scale
+    peak = hbm_peak if bound == "hbm" else bf16_peak
+    print(json.dumps({"case": case, "avg_us_per_call": us, "bound": bound, "achieved": ach,
+                      "unit": unit, "peak": peak, "frac": ach / peak, "peak_source": peak_src,
+                      "algorithmic_per_call": work, "steps": args.steps,
+                      "input_sets": len(sets)}), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.case != "mix":
+        return run_case(args)
     return run_gdn(args)
 
 

@@ -9,16 +9,16 @@
 //     A_rs = b_r e^{g_r-g_s} (k_r.k_s), P_rs = e^{g_r-g_s} (q_r.k_s)     (CUDA cores)
 //     Tm   = (I + A)^{-1}: one column per thread, forward substitution  (CUDA cores)
 //     W^T  = K^T (Tm diag(b e^g))^T,  U^T = V^T (Tm diag(b))^T          (M=128, N=64, K=64)
-//   and writes, per (chunk, v-head), a record with W (BF16 hi + lo), P, the
-//   scaled queries e^{g_r} q_r, K^T (all in the tile layout the state kernel
-//   feeds straight to the tensor core), U (float32) and g.
+//   and writes, per (chunk, v-head), a record with W (BF16 hi + lo) and P (in
+//   the tile layouts the state kernel feeds straight to the tensor core), U
+//   (float32) and the gates and norms.
 //
 //   state kernel, one CTA per (sequence, v-head), S [dv=128 x dk=128] float32
 //   resident in TMEM, chunks in order:
 //     X^T  = S W^T                  (S and W split into BF16 hi + lo: 3 MMAs)
-//     O^T  = S (e^g Q)^T            (single BF16: the output is BF16)
+//     O1^T = S Q^T                  (single BF16: the output is BF16)
 //     Delta^T = U^T - X^T           (CUDA cores, lane i holds row i)
-//     O^T += Delta^T P^T            (single BF16)
+//     O2^T = Delta^T P^T            (single BF16); o_r = e^{g_r} O1_r + O2_r
 //     S    = e^{g_last} S + (Delta^T diag(e^{g_last-g}))  K   (Delta split: 2 MMAs,
 //            accumulated onto the rescaled S in TMEM)
 //
@@ -42,16 +42,14 @@ constexpr int kC = 64;     // chunk tokens
 constexpr int kD = 128;    // head dim (dk = dv)
 constexpr int kThreads = 128;
 
-// Record of one (chunk, v-head) written by the chunk kernel.
-constexpr int kOffWhi = 0;          // W hi   [64 r][128 j] tile
+// Record of one (chunk, v-head) written by the chunk kernel and read, by bulk
+// copy, by the state kernel.
+constexpr int kOffWhi = 0;          // W hi   MN-major B tile: N = token r (64), K = j (128)
 constexpr int kOffWlo = 16384;      // W lo
-constexpr int kOffP = 32768;        // P      [64 r][64 s] tile
-constexpr int kOffGQ = 40960;       // e^g q  [64 r][128 j] tile
-constexpr int kOffKT = 57344;       // K^T    [128 j][64 s] tile
-constexpr int kTileBytes = 73728;   // the five tiles above, contiguous
-constexpr int kOffU = 73728;        // U      [128 i][64 r] float32 rows
-constexpr int kOffGK = 106496;      // g[64], rk[64] float32
-constexpr int kRecBytes = 107008;
+constexpr int kOffP = 32768;        // P      K-major  [64 r][64 s]
+constexpr int kOffU = 40960;        // U      [128 i][64 r] float32, 16-byte chunks XOR-swizzled
+constexpr int kOffGK = 73728;       // g[64] (log2 of the cumulative decay), rk[64], rq[64]
+constexpr int kRecBytes = 74496;    // 73728 + 768
 
 __host__ __device__ constexpr size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -69,42 +67,85 @@ __host__ __device__ inline TcLayout tc_layout(int T, int N, int Hv) {
   return L;
 }
 
-__device__ __forceinline__ void bf16_split(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-}
-
-// 8 floats -> hi and lo 16-byte vectors.
+// 8 floats -> BF16 hi and lo parts (hi = bf16(x), lo = bf16(x - hi)) as 16-byte vectors.
 __device__ __forceinline__ void split8(const float* f, uint4& hi, uint4& lo) {
-  float h[8], l[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    __nv_bfloat16 a, b;
-    bf16_split(f[e], a, b);
-    h[e] = __bfloat162float(a);
-    l[e] = __bfloat162float(b);
+  for (int e = 0; e < 4; ++e) {
+    h[e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
+    l[e] = pack_bf16x2(f[2 * e] - bf16lo(h[e]), f[2 * e + 1] - bf16hi(h[e]));
   }
-  hi = pack8(h);   // exact: values are already BF16
-  lo = pack8(l);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // ---------------------------------------------------------------------------
-// Chunk kernel
+// Chunk kernel: 128 threads, about 66 KB of shared memory and 128 TMEM columns,
+// so three CTAs share an SM.
 // ---------------------------------------------------------------------------
-// Shared memory map (bytes).
-constexpr int kS1_A1 = 0;          // [K;Q] tile [128][128]          32768
-constexpr int kS1_KT = 32768;      // K^T tile  [128 j][64 s]        16384
-constexpr int kS1_VT = 49152;      // V^T tile  [128 i][64 s]        16384
-constexpr int kS1_AF = 65536;      // A float32 [64][68] (rows 16-B aligned), also V staging
-constexpr int kS1_SM = kS1_AF + 64 * 68 * 4;   // g, b, rk, rq, cw: 5 x 64 floats
-constexpr int kS1_BAR = kS1_SM + 5 * 64 * 4;
+constexpr int kS1_A1 = 0;          // rows 0-63: K [s][j], rows 64-127: Q [r][j] (K-major, Kc 128)
+constexpr int kS1_V = 32768;       // V [s][i] (K-major layout, read as MN-major A for V^T)
+constexpr int kS1_AF = 49152;      // A float32 [64][68]
+constexpr int kS1_SM = kS1_AF + 64 * 68 * 4;   // g2, b, rk, rq, cw: 5 x 64 floats
+constexpr int kS1_RS = kS1_SM + 5 * 64 * 4;    // block-inverse scratch [3][16][16] float32
+constexpr int kS1_BAR = kS1_RS + 3 * 256 * 4;
 constexpr int kS1_BYTES = kS1_BAR + 64;
-// Aliases once [K;Q] has been consumed: Tm' hi/lo, Tm'' hi/lo tiles [64 r][64 s].
-constexpr int kS1_TWH = 0, kS1_TWL = 8192, kS1_TUH = 16384, kS1_TUL = 24576;
-// Aliases once the W/U products completed: W hi/lo staging tiles [64 r][128 j].
-constexpr int kS1_WST = 32768;
+// Tm float32 [64][64] in the Q rows once they are consumed; the MN-major B
+// tiles (N = r, K = s) of Tm diag(b e^g rk) go to the A area after the solve,
+// those of Tm diag(b) to the Q rows after Tm has been read.
+constexpr int kS1_TF = 16384;
+constexpr int kS1_TWH = kS1_AF, kS1_TWL = kS1_AF + 8192;
+constexpr int kS1_TUH = 16384, kS1_TUL = 24576;
 
-__global__ void __launch_bounds__(kThreads)
+// One distance of the blocked triangular inverse: for the tiles (i, j = i - D),
+// R_ij = sum_{s in [16 j, 16 i)} A[16 i + rr][s] Tm[s][16 j + cc], then
+// Tm_ij = -D_i R_ij. Each thread owns 2 (4 - D) outputs and carries them as
+// independent accumulators; trip counts are compile-time.
+template <int D>
+__device__ __forceinline__ void tm_offdiag(const float* __restrict__ Af, float* __restrict__ Tf,
+                                           float* __restrict__ Rs, int tid) {
+  constexpr int kOut = 2 * (4 - D);
+  float acc[kOut];
+#pragma unroll
+  for (int q = 0; q < kOut; ++q) acc[q] = 0.f;
+#pragma unroll
+  for (int s4 = 0; s4 < 16 * D; s4 += 4) {
+#pragma unroll
+    for (int q = 0; q < kOut; ++q) {
+      const int e = tid + 128 * q;
+      const int blk = e >> 8, i = D + blk, jb = i - D, rr = (e >> 4) & 15, cc = e & 15;
+      const int s0 = 16 * jb + s4;
+      const float4 a4 = *reinterpret_cast<const float4*>(Af + (16 * i + rr) * 68 + s0);
+      acc[q] = fmaf(a4.x, Tf[(s0 + 0) * 64 + 16 * jb + cc], acc[q]);
+      acc[q] = fmaf(a4.y, Tf[(s0 + 1) * 64 + 16 * jb + cc], acc[q]);
+      acc[q] = fmaf(a4.z, Tf[(s0 + 2) * 64 + 16 * jb + cc], acc[q]);
+      acc[q] = fmaf(a4.w, Tf[(s0 + 3) * 64 + 16 * jb + cc], acc[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kOut; ++q) Rs[tid + 128 * q] = acc[q];
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kOut; ++q) acc[q] = 0.f;
+#pragma unroll
+  for (int k2 = 0; k2 < 16; ++k2) {
+#pragma unroll
+    for (int q = 0; q < kOut; ++q) {
+      const int e = tid + 128 * q;
+      const int blk = e >> 8, i = D + blk, rr = (e >> 4) & 15, cc = e & 15;
+      acc[q] = fmaf(Tf[(16 * i + rr) * 64 + 16 * i + k2], Rs[blk * 256 + k2 * 16 + cc], acc[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kOut; ++q) {
+    const int e = tid + 128 * q;
+    const int blk = e >> 8, i = D + blk, jb = i - D, rr = (e >> 4) & 15, cc = e & 15;
+    Tf[(16 * i + rr) * 64 + 16 * jb + cc] = -acc[q];
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 3)
 tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ q,
                 int64_t qk_stride, const __nv_bfloat16* __restrict__ v, int64_t v_stride,
                 const float* __restrict__ a, const float* __restrict__ b,
@@ -131,19 +172,42 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
   const int h = blockIdx.y, gh = h / (Hv / Hk);
   unsigned char* rec = records + ((size_t)blockIdx.x * Hv + h) * kRecBytes;
 
+  // K, Q and V rows as 16-byte asynchronous copies, all in flight together.
+  // Lane l of a warp covers row (8 rg + l % 8) and chunk (4 kg + l / 8): eight
+  // consecutive rows per quarter warp keep the shared-memory writes
+  // conflict-free, four chunks per row keep the global reads in 64-byte runs.
+#pragma unroll
+  for (int it = 0; it < 16; ++it) {
+    const int p = it * 4 + warp;
+    const int row = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
+    const int rr = row & 63;
+    const bool valid = rr < n;
+    const __nv_bfloat16* src = (row < 64 ? k : q) + (int64_t)(tok0 + (valid ? rr : 0)) * qk_stride +
+                               (int64_t)gh * kD + kc * 8;
+    cp_async16(sm + kS1_A1 + tile_off(row, kc * 8, 128), src, valid ? 16u : 0u);
+  }
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int p = it * 4 + warp;
+    const int s = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
+    const bool valid = s < n;
+    cp_async16(sm + kS1_V + tile_off(s, kc * 8, 128),
+               v + (int64_t)(tok0 + (valid ? s : 0)) * v_stride + (int64_t)h * kD + kc * 8,
+               valid ? 16u : 0u);
+  }
   if (tid == 0) {
     mbar_init(mbar, 1);
     *s_fail = 0;
   }
   if (warp == 0) {
-    tmem_alloc(slot, 256);
+    tmem_alloc(slot, 128);
     tmem_relinquish();
   }
-
   // Gates: g = inclusive prefix sum of log a over the chunk (0 past the end).
   if (tid < 64) {
     const bool in = tid < n;
-    float x = in ? logf(fmaxf(a[(int64_t)(tok0 + tid) * Hv + h], 1e-30f)) : 0.f;
+    // log2 of the decay, so that decay ratios are single exp2 evaluations.
+    float x = in ? log2f(fmaxf(a[(int64_t)(tok0 + tid) * Hv + h], 1e-30f)) : 0.f;
     bs[tid] = in ? b[(int64_t)(tok0 + tid) * Hv + h] : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -153,170 +217,145 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
     if (tid == 31) *s_tot = x;
     gs[tid] = x;
   }
-  // [K; Q] rows into the A1 tile, with row sums of squares for the L2 norm.
-  for (int it = 0; it < 16; ++it) {
-    const int c = tid + kThreads * it;
-    const int row = c >> 4, kc = c & 15, rr = row & 63;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (rr < n) {
-      const __nv_bfloat16* src = (row < 64 ? k : q) + (int64_t)(tok0 + rr) * qk_stride +
-                                 (int64_t)gh * kD + kc * 8;
-      u = ldg16(src);
-    }
-    *reinterpret_cast<uint4*>(sm + kS1_A1 + tile_off(row, kc * 8, 128)) = u;
-    float f[8];
-    unpack8(u, f);
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ss += f[e] * f[e];
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (kc == 0) {
-      const float r = l2 ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-      if (row < 64) rk[rr] = r; else rq[rr] = r;
-    }
-  }
-  // V rows (plain row-major staging in the A area, 256 bytes per row).
-  for (int it = 0; it < 8; ++it) {
-    const int c = tid + kThreads * it;
-    const int s = c >> 4, kc = c & 15;
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (s < n) u = ldg16(v + (int64_t)(tok0 + s) * v_stride + (int64_t)h * kD + kc * 8);
-    *reinterpret_cast<uint4*>(sm + kS1_AF + s * 256 + kc * 16) = u;
-  }
+  cp_async_wait_all();
   __syncthreads();
   if (tid >= 32 && tid < 64) gs[tid] += *s_tot;
-  // K^T and V^T tiles [128][64]: thread -> (row j = tid, 8-token group it).
-  for (int it = 0; it < 8; ++it) {
-    const int j = tid;
-    float fk[8], fv[8];
+  // Row norms (thread = row; eight consecutive rows per quarter warp).
+  {
+    float ss = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int s = it * 8 + e;
-      fk[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-          sm + kS1_A1 + tile_off(s, j, 128)));
-      fv[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-          sm + kS1_AF + s * 256 + j * 2));
+    for (int kc = 0; kc < 16; ++kc) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(sm + kS1_A1 + tile_off(tid, kc * 8, 128)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
-    *reinterpret_cast<uint4*>(sm + kS1_KT + tile_off(j, it * 8, 64)) = pack8(fk);
-    *reinterpret_cast<uint4*>(sm + kS1_VT + tile_off(j, it * 8, 64)) = pack8(fv);
+    const float r = l2 ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    if (tid < 64) rk[tid] = r; else rq[tid - 64] = r;
   }
   fence_smem_to_async();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t taddr = *slot;
+  const uint32_t a1 = smem_u32(sm + kS1_A1);
 
-  // G = [K; Q] K^T  -> TMEM columns [0, 64).
+  // G = [K; Q] K^T -> TMEM columns [0, 64).
   if (tid == 0) {
-    const uint32_t a1 = smem_u32(sm + kS1_A1);
     for (int kk = 0; kk < 8; ++kk)
       mma_bf16(taddr, tile_desc(a1, 128, kk), tile_desc(a1, 128, kk), idesc_bf16_f32(128, 64),
                kk > 0);
     mma_commit(mbar);
   }
+  if (tid < 64) cw[tid] = bs[tid] * exp2f(gs[tid]) * rk[tid];
   if (!mbar_wait(mbar, 0)) atomicExch(s_fail, 1);
   fence_after_sync();
   {
-    float G0[32], G1[32];
-    tmem_ld32(tmem_warp_addr(taddr, 0), G0);
-    tmem_ld32(tmem_warp_addr(taddr, 32), G1);
-    if (tid < 64) {
-      const int r = tid;
-      const float br = bs[r] * rk[r], gr = gs[r];
+    // Row r of A = b_r e^{g_r - g_s} rk_r rk_s (k_r . k_s), strictly lower
+    // (threads 0-63), and row r of P = e^{g_r - g_s} rq_r rk_s (q_r . k_s),
+    // lower with the diagonal (threads 64-127); eight columns per step.
+    const bool is_a = tid < 64;
+    const int r = tid & 63;
+    const float gr = gs[r];
+    const float fr = is_a ? bs[r] * rk[r] : rq[r];
+#pragma unroll 1
+    for (int cb = 0; cb < 8; ++cb) {
+      float gv[8], v8[8];
+      tmem_ld8(tmem_warp_addr(taddr, 8 * cb), gv);
 #pragma unroll
-      for (int s0 = 0; s0 < 64; s0 += 4) {
-        float o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int s = s0 + e;
-          const float gv = s < 32 ? G0[s & 31] : G1[s & 31];
-          o[e] = (s < r && r < n) ? br * expf(gr - gs[s]) * rk[s] * gv : 0.f;
-        }
-        *reinterpret_cast<float4*>(Af + r * 68 + s0) = make_float4(o[0], o[1], o[2], o[3]);
+      for (int e = 0; e < 8; ++e) {
+        const int s2 = 8 * cb + e;
+        const bool keep = (is_a ? s2 < r : s2 <= r) && r < n;
+        v8[e] = keep ? fr * exp2f(gr - gs[s2]) * rk[s2] * gv[e] : 0.f;
       }
-    } else {
-      const int r = tid - 64;
-      const float qr = rq[r], gr = gs[r];
-#pragma unroll
-      for (int s0 = 0; s0 < 64; s0 += 8) {
-        float pv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = s0 + e;
-          const float gv = s < 32 ? G0[s & 31] : G1[s & 31];
-          pv[e] = (s <= r && r < n) ? expf(gr - gs[s]) * qr * rk[s] * gv : 0.f;
-        }
-        *reinterpret_cast<uint4*>(rec + kOffP + tile_off(r, s0, 64)) = pack8(pv);
+      if (is_a) {
+        *reinterpret_cast<float4*>(Af + r * 68 + 8 * cb) = make_float4(v8[0], v8[1], v8[2], v8[3]);
+        *reinterpret_cast<float4*>(Af + r * 68 + 8 * cb + 4) = make_float4(v8[4], v8[5], v8[6], v8[7]);
+      } else {
+        *reinterpret_cast<uint4*>(rec + kOffP + tile_off(r, 8 * cb, 64)) = pack8(v8);
       }
     }
   }
-  // e^{g_r} rq_r q_r tile and K^T tile to the record.
-  for (int it = 0; it < 8; ++it) {
-    const int c = tid + kThreads * it;
-    const int r = c >> 4, kc = c & 15;
-    const uint4 u = *reinterpret_cast<const uint4*>(sm + kS1_A1 + tile_off(64 + r, kc * 8, 128));
-    const float sc = r < n ? expf(gs[r]) * rq[r] : 0.f;
-    float f[8];
-    unpack8(u, f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] *= sc;
-    *reinterpret_cast<uint4*>(rec + kOffGQ + tile_off(r, kc * 8, 128)) = pack8(f);
-  }
-  for (int it = 0; it < 8; ++it) {
-    const int c = tid + kThreads * it;
-    reinterpret_cast<uint4*>(rec + kOffKT)[c] = reinterpret_cast<const uint4*>(sm + kS1_KT)[c];
-  }
-  if (tid < 64) cw[tid] = bs[tid] * expf(gs[tid]) * rk[tid];
   fence_before_sync();
   __syncthreads();
 
-  // Tm = (I + A)^{-1}: thread t solves column j = t % 64 by forward substitution
-  // (x_r = -sum_{s<r} A_rs x_s, x_j = 1); threads 0-63 write the W-side tiles
-  // (Tm diag(b e^g rk)), threads 64-127 the U-side tiles (Tm diag(b)).
-  {
-    const int j = tid & 63;
-    float x[64];
+  // Tm = (I + A)^{-1}, blocked in 16 x 16 tiles. Diagonal tiles D_i =
+  // (I + A_ii)^{-1} by forward substitution (thread = column); then, for
+  // i - j = 1, 2, 3: Tm_ij = -D_i R_ij with R_ij = sum_{s in [16j, 16i)} A[., s] Tm[s, .]
+  // (Tm is zero above the diagonal, so the sum runs over one contiguous range).
+  float* Tf = reinterpret_cast<float*>(sm + kS1_TF);   // [64][64]
+  float* Rs = reinterpret_cast<float*>(sm + kS1_RS);   // [3][16][16]
+  if (tid < 64) {
+    const int bi = tid >> 4, c = tid & 15, o0 = 16 * bi;
+    float x[16];
 #pragma unroll
-    for (int r = 0; r < 64; ++r) x[r] = 0.f;
+    for (int r = 0; r < 16; ++r) {
+      float acc = 0.f;
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-      for (int s = 0; s < r; s += 4) {
-        const float4 a4 = *reinterpret_cast<const float4*>(Af + r * 68 + s);
-        acc0 = fmaf(a4.x, x[s], acc0);
-        acc1 = fmaf(a4.y, x[s + 1], acc1);
-        acc0 = fmaf(a4.z, x[s + 2], acc0);
-        acc1 = fmaf(a4.w, x[s + 3], acc1);
-      }
-      x[r] = (r == j) ? 1.f : -(acc0 + acc1);
+      for (int s2 = 0; s2 < r; ++s2) acc = fmaf(Af[(o0 + r) * 68 + o0 + s2], x[s2], acc);
+      x[r] = (r == c) ? 1.f : (r < c ? 0.f : -acc);
     }
-    const float scale = (tid < 64) ? cw[j] : bs[j];
-    unsigned char* th = sm + (tid < 64 ? kS1_TWH : kS1_TUH);
-    unsigned char* tl = sm + (tid < 64 ? kS1_TWL : kS1_TUL);
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      __nv_bfloat16 hi, lo;
-      bf16_split(x[r] * scale, hi, lo);
-      *reinterpret_cast<__nv_bfloat16*>(th + tile_off(r, j, 64)) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(tl + tile_off(r, j, 64)) = lo;
+    for (int r = 0; r < 16; ++r) Tf[(o0 + r) * 64 + o0 + c] = x[r];
+  } else {
+    // zero the strictly upper tiles (i < j): 6 tiles of 256
+    for (int e = tid - 64; e < 6 * 256; e += 64) {
+      const int t6 = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+      const int ti = t6 < 3 ? 0 : (t6 < 5 ? 1 : 2);
+      const int tj = t6 < 3 ? t6 + 1 : (t6 < 5 ? t6 - 1 : 3);
+      Tf[(16 * ti + rr) * 64 + 16 * tj + cc] = 0.f;
+    }
+  }
+  __syncthreads();
+  tm_offdiag<1>(Af, Tf, Rs, tid);
+  tm_offdiag<2>(Af, Tf, Rs, tid);
+  tm_offdiag<3>(Af, Tf, Rs, tid);
+  // B tiles: column s of Tm diag(b e^g rk) and of Tm diag(b), split hi/lo, as
+  // MN-major tiles (N = r, K = s): eight consecutive r per 16 bytes. The W-side
+  // tiles go to the (now free) A area at once; the U-side ones are held in
+  // registers until every thread is done reading Tm, then overwrite it.
+  {
+    uint4 uh[4], ul[4];
+    const int s_ = tid & 63, rg0 = (tid >> 6) * 4;
+    const float cws = cw[s_], bss = bs[s_];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int rg = rg0 + q4;
+      float t8[8], f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t8[e] = Tf[(8 * rg + e) * 64 + s_];
+      uint4 hi, lo;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = t8[e] * cws;
+      split8(f, hi, lo);
+      *reinterpret_cast<uint4*>(sm + kS1_TWH + mn_off(8 * rg, s_, 64)) = hi;
+      *reinterpret_cast<uint4*>(sm + kS1_TWL + mn_off(8 * rg, s_, 64)) = lo;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = t8[e] * bss;
+      split8(f, uh[q4], ul[q4]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int rg = rg0 + q4;
+      *reinterpret_cast<uint4*>(sm + kS1_TUH + mn_off(8 * rg, s_, 64)) = uh[q4];
+      *reinterpret_cast<uint4*>(sm + kS1_TUL + mn_off(8 * rg, s_, 64)) = ul[q4];
     }
   }
   fence_smem_to_async();
   __syncthreads();
   fence_after_sync();
 
-  // W^T = K^T Tm'^T -> cols [64, 128);  U^T = V^T Tm''^T -> cols [128, 192).
+  // W^T = K^T Tm'^T -> cols [0, 64);  U^T = V^T Tm''^T -> cols [64, 128).
   if (tid == 0 && !*s_fail) {
-    const uint32_t kt = smem_u32(sm + kS1_KT), vt = smem_u32(sm + kS1_VT);
+    const uint32_t vt = smem_u32(sm + kS1_V);
     const uint32_t twh = smem_u32(sm + kS1_TWH), twl = smem_u32(sm + kS1_TWL);
     const uint32_t tuh = smem_u32(sm + kS1_TUH), tul = smem_u32(sm + kS1_TUL);
-    const uint32_t id = idesc_bf16_f32(128, 64);
-    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 64, tile_desc(kt, 64, kk), tile_desc(twh, 64, kk), id, kk > 0);
-    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 64, tile_desc(kt, 64, kk), tile_desc(twl, 64, kk), id, 1);
-    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 128, tile_desc(vt, 64, kk), tile_desc(tuh, 64, kk), id, kk > 0);
-    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 128, tile_desc(vt, 64, kk), tile_desc(tul, 64, kk), id, 1);
+    const uint32_t id = idesc_bf16_f32(128, 64) | kTransA | kTransB;
+    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, mn_desc(a1, 128, kk), mn_desc(twh, 64, kk), id, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, mn_desc(a1, 128, kk), mn_desc(twl, 64, kk), id, 1);
+    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 64, mn_desc(vt, 128, kk), mn_desc(tuh, 64, kk), id, kk > 0);
+    for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 64, mn_desc(vt, 128, kk), mn_desc(tul, 64, kk), id, 1);
     mma_commit(mbar);
   }
   __syncthreads();
@@ -326,79 +365,108 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
   fence_after_sync();
   __syncthreads();
   if (!*s_fail) {
-    // Lane j holds W[r][j] for all r: split into the staging tiles [64 r][128 j].
+    // Stage the record in shared memory in its global layout (W hi/lo over the
+    // consumed K/Q rows, U over V and the A area, gates over the scratch), then
+    // write it with three bulk stores.
+    // Lane j holds W[r][j] for all r: MN-major B tiles (N = r, K = j).
     float w[32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld32(tmem_warp_addr(taddr, 32 * half), w);
+#pragma unroll
+      for (int rg = 0; rg < 4; ++rg) {
+        uint4 hi, lo;
+        split8(w + 8 * rg, hi, lo);
+        const uint32_t off = mn_off(32 * half + 8 * rg, tid, 64);
+        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffWhi + off) = hi;
+        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffWlo + off) = lo;
+      }
+    }
+    // Lane i holds U[r][i] for all r: row i (float32), its 16-byte chunk c at
+    // position c ^ (i % 8) so that the state kernel reads one chunk per row
+    // across a warp without bank conflicts.
+    float4* urow = reinterpret_cast<float4*>(sm + kS1_V) + tid * 16;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       tmem_ld32(tmem_warp_addr(taddr, 64 + 32 * half), w);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = 32 * half + e;
-        __nv_bfloat16 hi, lo;
-        bf16_split(w[e], hi, lo);
-        *reinterpret_cast<__nv_bfloat16*>(sm + kS1_WST + tile_off(r, tid, 128)) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(sm + kS1_WST + 16384 + tile_off(r, tid, 128)) = lo;
-      }
-    }
-    // Lane i holds U[r][i] for all r: row i of the U record (float32).
-    float* urow = reinterpret_cast<float*>(rec + kOffU) + tid * 64;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tmem_warp_addr(taddr, 128 + 32 * half), w);
-#pragma unroll
       for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(urow + 32 * half + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+        urow[(8 * half + e / 4) ^ (tid & 7)] = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
     }
     if (tid < 64) {
-      float* gk = reinterpret_cast<float*>(rec + kOffGK);
-      gk[tid] = gs[tid];
+      float* gk = reinterpret_cast<float*>(sm + kS1_RS);
+      gk[tid] = gs[tid];          // log2 units
       gk[64 + tid] = rk[tid];
+      gk[128 + tid] = rq[tid];
     }
-  }
-  fence_before_sync();
-  __syncthreads();
-  if (!*s_fail) {
-    for (int it = 0; it < 16; ++it) {
-      const int c = tid + kThreads * it;
-      reinterpret_cast<uint4*>(rec + kOffWhi)[c] =
-          reinterpret_cast<const uint4*>(sm + kS1_WST)[c];
-    }
+    fence_smem_to_async();
   } else if (tid == 0) {
     atomicExch(status + 2, (int)GDN_ERR_TIMEOUT);
   }
-  if (warp == 0) tmem_dealloc(taddr, 256);
+  fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && !*s_fail) {
+    bulk_s2g(rec + kOffWhi, sm + kS1_A1 + kOffWhi, 32768);
+    bulk_s2g(rec + kOffU, sm + kS1_V, 32768);
+    bulk_s2g(rec + kOffGK, sm + kS1_RS, 768);
+    bulk_commit();
+    bulk_wait_all();
+  }
+  if (warp == 0) tmem_dealloc(taddr, 128);
 }
 
 // ---------------------------------------------------------------------------
-// State kernel
+// State kernel: 256 threads. Warp w reads TMEM lanes 32 (w % 4) .. + 31 (row
+// i = lane of that quarter) and handles column half w / 4 of every row-wise
+// step, so each step is split over two warps per row.
+// TMEM: S in columns [0, 128), X^T in [128, 192), O1^T and O2^T double-buffered
+// in [256, 384) and [384, 512): a chunk's outputs are written back while the
+// next chunk's first MMA round runs.
+// Per chunk, the record arrives in three bulk copies issued as soon as the
+// buffer they refill is free (W and gates after the first MMA round, U after
+// Delta, P after the second round), and the raw Q and K rows of the next chunk
+// in 16-byte asynchronous copies as soon as their tiles are free.
 // ---------------------------------------------------------------------------
+constexpr int kThreads2 = 256;
 constexpr int kS2_SAH = 0;          // S hi  [128 i][128 j]   32768
 constexpr int kS2_SAL = 32768;      // S lo                   32768
-constexpr int kS2_DA = 65536;       // Delta^T hi [128 i][64 s] 16384
-constexpr int kS2_DDH = 81920;      // (Delta^T D) hi           16384
-constexpr int kS2_DDL = 98304;      // (Delta^T D) lo           16384
-constexpr int kS2_B = 114688;       // record tiles (Whi, Wlo, P, GQ, KT) 73728
-constexpr int kS2_WH = kS2_B + kOffWhi, kS2_WL = kS2_B + kOffWlo, kS2_P = kS2_B + kOffP;
-constexpr int kS2_GQ = kS2_B + kOffGQ, kS2_KT = kS2_B + kOffKT;
-constexpr int kS2_GK = kS2_B + kTileBytes;        // g[64], rk[64]
-constexpr int kS2_DK = kS2_GK + 512;              // D_s rk_s [64]
-constexpr int kS2_BAR = kS2_DK + 256;
+constexpr int kS2_DA = 65536;       // Delta^T [128 i][64 s]  16384
+constexpr int kS2_DDH = 81920;      // (Delta^T D) hi         16384
+constexpr int kS2_DDL = 98304;      // (Delta^T D) lo         16384
+constexpr int kS2_Q = 114688;       // Q rows [64 r][128 j] K-major B   16384
+constexpr int kS2_K = 131072;       // K rows [64 s][128 j] (MN-major B) 16384
+constexpr int kS2_R = 147456;       // the chunk's record
+constexpr int kS2_WH = kS2_R + kOffWhi, kS2_WL = kS2_R + kOffWlo, kS2_P = kS2_R + kOffP;
+constexpr int kS2_U = kS2_R + kOffU, kS2_GK = kS2_R + kOffGK;
+constexpr int kS2_QS = kS2_R + kRecBytes;         // e^{g_r} rq_r, two chunks [2][64]
+constexpr int kS2_DK = kS2_QS + 512;              // e^{g_last - g_s} rk_s [64]
+constexpr int kS2_BAR = kS2_DK + 256;             // barriers, TMEM slot, ...
 constexpr int kS2_BYTES = kS2_BAR + 64;
 
-__global__ void __launch_bounds__(kThreads, 1)
-tc_state_kernel(const int32_t* __restrict__ cu, int T, int N, float* __restrict__ S,
-                const uint8_t* __restrict__ has_init, __nv_bfloat16* __restrict__ o, int Hv,
-                const unsigned char* __restrict__ records, int32_t* __restrict__ hdr) {
+__global__ void __launch_bounds__(kThreads2, 1)
+tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                int64_t qk_stride, const int32_t* __restrict__ cu, int T, int Hk,
+                float* __restrict__ S, const uint8_t* __restrict__ has_init,
+                __nv_bfloat16* __restrict__ o, int Hv, const unsigned char* __restrict__ records,
+                int32_t* __restrict__ hdr) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  float* gk = reinterpret_cast<float*>(sm + kS2_GK);
+  const float* gk = reinterpret_cast<const float*>(sm + kS2_GK);
+  const float4* us = reinterpret_cast<const float4*>(sm + kS2_U);
+  float* qs = reinterpret_cast<float*>(sm + kS2_QS);
   float* dks = reinterpret_cast<float*>(sm + kS2_DK);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kS2_BAR);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 8);
-  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 12);
-  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 16);
+  uint64_t* tbA = mbar + 1;   // W hi/lo + gates
+  uint64_t* tbU = mbar + 2;   // U
+  uint64_t* tbB = mbar + 3;   // P
+  uint64_t* obar = mbar + 4;  // a chunk's output MMAs
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 40);
+  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 44);
+  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 48);
 
-  const int seq = blockIdx.x, h = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int seq = blockIdx.x, h = blockIdx.y, gh = h / (Hv / Hk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = 32 * (warp & 3) + lane;   // S row (dv index) = TMEM lane
+  const int hf = warp >> 2;                 // column / token half
   const int start = cu[seq], end = cu[seq + 1];
   if (start < 0 || end <= start || end > T) return;
   const int nchunks = (end - start + kC - 1) / kC;
@@ -407,18 +475,22 @@ tc_state_kernel(const int32_t* __restrict__ cu, int T, int N, float* __restrict_
     *s_first = 0;
     *s_fail = 0;
     mbar_init(mbar, 1);
+    mbar_init(tbA, 1);
+    mbar_init(tbU, 1);
+    mbar_init(tbB, 1);
+    mbar_init(obar, 1);
   }
   __syncthreads();
   {
     int cnt = 0;
-    for (int s = tid; s < seq; s += kThreads) {
+    for (int s = tid; s < seq; s += kThreads2) {
       const int L = cu[s + 1] - cu[s];
       if (L > 0) cnt += (L + kC - 1) / kC;
     }
     if (cnt) atomicAdd(s_first, cnt);
   }
   if (warp == 0) {
-    tmem_alloc(slot, 256);
+    tmem_alloc(slot, 512);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -428,153 +500,256 @@ tc_state_kernel(const int32_t* __restrict__ cu, int T, int N, float* __restrict_
   const int first = *s_first;
   const bool records_ok = first + nchunks <= hdr[0];
 
-  float* Sg = S + (((size_t)seq * Hv + h) * kD + tid) * kD;
+  float* Sg = S + (((size_t)seq * Hv + h) * kD + row) * kD;
   const bool init = has_init != nullptr && has_init[seq] != 0;
-  {
-    float vbuf[32];
-    for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        float4 f4 = init ? *reinterpret_cast<const float4*>(Sg + blk * 32 + e)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        vbuf[e] = f4.x; vbuf[e + 1] = f4.y; vbuf[e + 2] = f4.z; vbuf[e + 3] = f4.w;
-      }
-      tmem_st32(tmem_warp_addr(taddr, blk * 32), vbuf);
+  for (int blk = 0; blk < 2; ++blk) {
+    const int c0 = 64 * hf + 32 * blk;
+    float vbuf[32];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 f4 = init ? *reinterpret_cast<const float4*>(Sg + c0 + e)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+      vbuf[e] = f4.x; vbuf[e + 1] = f4.y; vbuf[e + 2] = f4.z; vbuf[e + 3] = f4.w;
     }
+    tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
   }
 
-  uint32_t phase = 0;
+  auto rec_of = [&](int ci) {
+    return records + ((size_t)(first + ci) * Hv + h) * kRecBytes;
+  };
+  // Outstanding record copies (thread 0's view), for the bounded drain on exit.
+  int pend_a = -1, pend_u = -1, pend_b = -1;
+  auto copy_a = [&](int ci) {
+    const unsigned char* rec = rec_of(ci);
+    mbar_arrive_expect_tx(tbA, 32768 + 768);
+    bulk_g2s(sm + kS2_WH, rec + kOffWhi, 16384, tbA);
+    bulk_g2s(sm + kS2_WL, rec + kOffWlo, 16384, tbA);
+    bulk_g2s(sm + kS2_GK, rec + kOffGK, 768, tbA);
+    pend_a = ci;
+  };
+  auto copy_u = [&](int ci) {
+    mbar_arrive_expect_tx(tbU, 32768);
+    bulk_g2s(sm + kS2_U, rec_of(ci) + kOffU, 32768, tbU);
+    pend_u = ci;
+  };
+  auto copy_b = [&](int ci) {
+    mbar_arrive_expect_tx(tbB, 8192);
+    bulk_g2s(sm + kS2_P, rec_of(ci) + kOffP, 8192, tbB);
+    pend_b = ci;
+  };
+  // Raw Q (or K) rows of chunk ci into their tile: one committed group per call
+  // (empty past the last chunk, so group counting stays uniform).
+  auto load_rows = [&](int ci, const __nv_bfloat16* src, int tile) {
+    if (ci < nchunks) {
+      const int c0 = start + ci * kC;
+      const int n = min(kC, end - c0);
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int p = it * 8 + warp;
+        const int r = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
+        const bool valid = r < n;
+        cp_async16(sm + tile + tile_off(r, kc * 8, 128),
+                   src + (int64_t)(c0 + (valid ? r : 0)) * qk_stride + (int64_t)gh * kD + kc * 8,
+                   valid ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
+  };
+  if (records_ok && nchunks > 0) {
+    if (tid == 0) {
+      copy_a(0);
+      copy_u(0);
+      copy_b(0);
+    }
+    load_rows(0, q, kS2_Q);
+    load_rows(0, k, kS2_K);
+  }
+
+  // Output write-back of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r, done by
+  // warps 4-7 only (warp 4 + q reads TMEM lanes 32q..32q+31, i.e. rows i, all
+  // 64 token columns), so warps 0-3 (warp 0 issues the MMAs) never wait for
+  // it. The values go through a [64 r][128 i] BF16 staging tile in the Delta^T
+  // area (unused at this point; the callers put a block-wide barrier before
+  // the area is written again) and leave as 16-byte vectors along dv.
+  auto write_outputs = [&](int cj) {
+    const int c0 = start + cj * kC;
+    const int n = min(kC, end - c0);
+    const float* qsb = qs + 64 * (cj & 1);
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + kS2_DA);
+    if (!mbar_wait(obar, cj & 1)) atomicExch(s_fail, 1);
+    fence_after_sync();
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float o1[32], o2[32];
+      tmem_ld32(tmem_warp_addr(taddr, 256 + 64 * (cj & 1) + 32 * half), o1);
+      tmem_ld32(tmem_warp_addr(taddr, 384 + 64 * (cj & 1) + 32 * half), o2);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int r = 32 * half + e;
+        stage[r * kD + row] = __float2bfloat16_rn(fmaf(o1[e], qsb[r], o2[e]));
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");   // warps 4-7 only
+    const int t = tid - 128;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int c = t + 128 * it;          // 16-byte chunk: token c / 16, dims 8 (c % 16)
+      const int r = c >> 4;
+      if (r < n)
+        *reinterpret_cast<uint4*>(o + ((int64_t)(c0 + r) * Hv + h) * kD + (c & 15) * 8) =
+            reinterpret_cast<const uint4*>(stage)[c];
+    }
+  };
+
   const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
+  uint32_t phase = 0;
+  int done = 0;   // chunks whose MMAs completed (their outputs may still be pending)
   for (int ci = 0; ci < nchunks && records_ok; ++ci) {
     const int c0 = start + ci * kC;
     const int n = min(kC, end - c0);
-    const unsigned char* rec = records + ((size_t)(first + ci) * Hv + h) * kRecBytes;
-    // (a) this chunk's tiles, gates and U row.
-    for (int it = 0; it < kTileBytes / 16 / kThreads; ++it) {
-      const int c = tid + kThreads * it;
-      reinterpret_cast<uint4*>(sm + kS2_B)[c] = __ldg(reinterpret_cast<const uint4*>(rec) + c);
-    }
-    if (tid < 32)
-      reinterpret_cast<uint4*>(sm + kS2_GK)[tid] =
-          __ldg(reinterpret_cast<const uint4*>(rec + kOffGK) + tid);
-    float u[64];
-    {
-      const float4* up = reinterpret_cast<const float4*>(rec + kOffU) + tid * 16;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float4 f = __ldg(up + e);
-        u[4 * e] = f.x; u[4 * e + 1] = f.y; u[4 * e + 2] = f.z; u[4 * e + 3] = f.w;
-      }
-    }
-    __syncthreads();
+    const uint32_t par = ci & 1;
+    const uint32_t o1col = 256 + 64 * par, o2col = 384 + 64 * par;
+    if (!mbar_wait(tbA, par)) atomicExch(s_fail, 1);
+    if (tid == 0) pend_a = -1;
     const float glast = gk[n - 1];
-    const float gamma_c = expf(glast);
-    if (tid < 64) dks[tid] = tid < n ? expf(glast - gk[tid]) * gk[64 + tid] : 0.f;
-    // (b) S -> hi/lo A tiles (row i = tid), then S <- e^{g_last} S in TMEM.
-    for (int blk = 0; blk < 4; ++blk) {
+    const float gamma_c = exp2f(glast);
+    if (tid < 64) {
+      const bool in = tid < n;
+      dks[tid] = in ? exp2f(glast - gk[tid]) * gk[64 + tid] : 0.f;
+      qs[64 * par + tid] = in ? exp2f(gk[tid]) * gk[128 + tid] : 0.f;
+    }
+    // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const int cb = 64 * hf + 32 * blk;
       float sv[32];
-      tmem_ld32(tmem_warp_addr(taddr, blk * 32), sv);
+      tmem_ld32(tmem_warp_addr(taddr, cb), sv);
 #pragma unroll
       for (int e8 = 0; e8 < 4; ++e8) {
         uint4 hi, lo;
         split8(sv + 8 * e8, hi, lo);
-        const int j0 = blk * 32 + e8 * 8;
-        *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(tid, j0, 128)) = hi;
-        *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(tid, j0, 128)) = lo;
+        *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb + 8 * e8, 128)) = hi;
+        *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb + 8 * e8, 128)) = lo;
       }
 #pragma unroll
       for (int e = 0; e < 32; ++e) sv[e] *= gamma_c;
-      tmem_st32(tmem_warp_addr(taddr, blk * 32), sv);
+      tmem_st32(tmem_warp_addr(taddr, cb), sv);
     }
+    cp_async_wait_group<1>();   // this chunk's Q rows (its K rows may still be landing)
     fence_smem_to_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // (c) X^T = S W^T (3 passes) -> cols [128,192);  O^T = S (e^g Q)^T -> cols [192,256).
+    // (c) X^T = S W^T (3 passes) -> cols [128, 192);  O1^T = S Q^T -> o1col.
     if (tid == 0) {
       const uint32_t sah = smem_u32(sm + kS2_SAH), sal = smem_u32(sm + kS2_SAL);
       const uint32_t wh = smem_u32(sm + kS2_WH), wl = smem_u32(sm + kS2_WL);
-      const uint32_t gq = smem_u32(sm + kS2_GQ);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), tile_desc(wh, 128, kk), id64, kk > 0);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), tile_desc(wl, 128, kk), id64, 1);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), tile_desc(wh, 128, kk), id64, 1);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 192, tile_desc(sah, 128, kk), tile_desc(gq, 128, kk), id64, kk > 0);
-      mma_commit(mbar);
+      const uint32_t qt = smem_u32(sm + kS2_Q);
+      const uint32_t idw = id64 | kTransB;
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(wh, 64, kk), idw, kk > 0);
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(wl, 64, kk), idw, 1);
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(wh, 64, kk), idw, 1);
+      mma_commit(mbar);   // X is what Delta waits for; O1 completes with the output barrier
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
     }
+    // Warps 4-7 write the previous chunk's outputs while these MMAs run.
+    if (done > 0 && warp >= 4) write_outputs(ci - 1);
     if (!mbar_wait(mbar, phase)) atomicExch(s_fail, 1);
     phase ^= 1;
     fence_after_sync();
-    // (d) Delta^T = U^T - X^T for this lane's row i; A tiles for O and for S.
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    // W, the gates and the Q tile are free: fetch the next chunk's.
+    if (tid == 0 && ci + 1 < nchunks) copy_a(ci + 1);
+    load_rows(ci + 1, q, kS2_Q);
+    if (!mbar_wait(tbU, par)) atomicExch(s_fail, 1);
+    if (tid == 0) pend_u = -1;
+    fence_before_sync();
+    __syncthreads();   // the output staging in the Delta^T area has been read
+    // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
+    {
       float xv[32];
-      tmem_ld32(tmem_warp_addr(taddr, 128 + 32 * half), xv);
+      tmem_ld32(tmem_warp_addr(taddr, 128 + 32 * hf), xv);
 #pragma unroll
       for (int e8 = 0; e8 < 4; ++e8) {
+        const float4 u0 = us[row * 16 + ((8 * hf + 2 * e8) ^ (row & 7))];
+        const float4 u1 = us[row * 16 + ((8 * hf + 2 * e8 + 1) ^ (row & 7))];
+        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         float dl[8], dd[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int r = 32 * half + 8 * e8 + e;
-          const float del = r < n ? u[r] - xv[8 * e8 + e] : 0.f;
+          const int r = 32 * hf + 8 * e8 + e;
+          const float del = r < n ? uu[e] - xv[8 * e8 + e] : 0.f;
           dl[e] = del;
           dd[e] = del * dks[r];
         }
-        const int s0 = 32 * half + 8 * e8;
+        const int s0 = 32 * hf + 8 * e8;
         uint4 hi, lo;
-        *reinterpret_cast<uint4*>(sm + kS2_DA + tile_off(tid, s0, 64)) = pack8(dl);
+        *reinterpret_cast<uint4*>(sm + kS2_DA + tile_off(row, s0, 64)) = pack8(dl);
         split8(dd, hi, lo);
-        *reinterpret_cast<uint4*>(sm + kS2_DDH + tile_off(tid, s0, 64)) = hi;
-        *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(tid, s0, 64)) = lo;
+        *reinterpret_cast<uint4*>(sm + kS2_DDH + tile_off(row, s0, 64)) = hi;
+        *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(row, s0, 64)) = lo;
       }
     }
+    cp_async_wait_group<1>();   // this chunk's K rows (the next Q rows may still be landing)
     fence_smem_to_async();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // (e) O^T += Delta^T P^T;  S += (Delta^T D) K  (hi and lo passes).
-    if (tid == 0 && !*s_fail) {
-      const uint32_t da = smem_u32(sm + kS2_DA), p = smem_u32(sm + kS2_P);
-      const uint32_t ddh = smem_u32(sm + kS2_DDH), ddl = smem_u32(sm + kS2_DDL);
-      const uint32_t kt = smem_u32(sm + kS2_KT);
-      for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 192, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, 1);
-      for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), tile_desc(kt, 64, kk), id128, 1);
-      for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), tile_desc(kt, 64, kk), id128, 1);
-      mma_commit(mbar);
+    // (e) O2^T = Delta^T P^T;  S += (Delta^T D) K  (hi and lo passes).
+    if (tid == 0) {
+      if (ci + 1 < nchunks) copy_u(ci + 1);     // every thread is done with this U
+      if (!mbar_wait(tbB, par)) atomicExch(s_fail, 1);
+      pend_b = -1;
+      if (!*s_fail) {
+        const uint32_t da = smem_u32(sm + kS2_DA), p = smem_u32(sm + kS2_P);
+        const uint32_t ddh = smem_u32(sm + kS2_DDH), ddl = smem_u32(sm + kS2_DDL);
+        const uint32_t kt = smem_u32(sm + kS2_K);
+        const uint32_t idk = id128 | kTransB;
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), mn_desc(kt, 128, kk), idk, 1);
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), mn_desc(kt, 128, kk), idk, 1);
+        mma_commit(mbar);   // the next chunk needs only S
+        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + o2col, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, kk > 0);
+        mma_commit(obar);
+      }
     }
     __syncthreads();
     if (*s_fail) break;
     if (!mbar_wait(mbar, phase)) atomicExch(s_fail, 1);
     phase ^= 1;
     fence_after_sync();
-    // (f) outputs: lane i holds O[r][i] for the chunk's tokens r.
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float ov[32];
-      tmem_ld32(tmem_warp_addr(taddr, 192 + 32 * half), ov);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = 32 * half + e;
-        if (r < n) o[((int64_t)(c0 + r) * Hv + h) * kD + tid] = __float2bfloat16_rn(ov[e]);
-      }
-    }
+    done = ci + 1;
+    // P and the K tile are free: fetch the next chunk's.
+    if (tid == 0 && ci + 1 < nchunks) copy_b(ci + 1);
+    load_rows(ci + 1, k, kS2_K);
     fence_before_sync();
     __syncthreads();
     if (*s_fail) break;
   }
+  cp_async_wait_all();
   if (!*s_fail && records_ok) {
-    for (int blk = 0; blk < 4; ++blk) {
+    if (done > 0 && warp >= 4) write_outputs(done - 1);
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const int cb = 64 * hf + 32 * blk;
       float sv[32];
-      tmem_ld32(tmem_warp_addr(taddr, blk * 32), sv);
+      tmem_ld32(tmem_warp_addr(taddr, cb), sv);
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(Sg + blk * 32 + e) = make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
+        *reinterpret_cast<float4*>(Sg + cb + e) = make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
     }
   } else if (tid == 0) {
     atomicExch(hdr + 2, (int)(*s_fail ? GDN_ERR_TIMEOUT : GDN_ERR_INVALID_ARG));
   }
+  // After an early exit, record copies may still be landing: wait (bounded)
+  // for them before the CTA's shared memory is released.
+  if (tid == 0) {
+    if (pend_a >= 0) mbar_wait(tbA, pend_a & 1);
+    if (pend_u >= 0) mbar_wait(tbU, pend_u & 1);
+    if (pend_b >= 0) mbar_wait(tbB, pend_b & 1);
+  }
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(taddr, 256);
+  if (warp == 0) tmem_dealloc(taddr, 512);
 }
 
 }  // namespace
@@ -607,8 +782,9 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
       static_cast<const __nv_bfloat16*>(v), v_stride, a, b, hdr, desc, T, Hk, Hv, qk_l2norm,
       records, hdr);
   if ((rc = check_launch()) != GDN_OK) return rc;
-  tc_state_kernel<<<dim3(N, Hv), kThreads, kS2_BYTES, st>>>(
-      cu, T, N, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, records, hdr);
+  tc_state_kernel<<<dim3(N, Hv), kThreads2, kS2_BYTES, st>>>(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride, cu,
+      T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, records, hdr);
   return check_launch();
 }
 

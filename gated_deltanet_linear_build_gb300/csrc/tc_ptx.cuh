@@ -44,6 +44,24 @@ __device__ __forceinline__ uint64_t tile_desc(uint32_t tile_addr, int Kc, int kk
                    128u, (uint32_t)(Kc * 16));
 }
 
+// MN-major ("transposed") tile of R rows along M or N by Kc along K: core
+// matrices are 8 K-rows x 16 bytes along MN; MN-adjacent core matrices are 128
+// bytes apart (stride-dimension offset) and K-adjacent ones R * 16 bytes apart
+// (leading-dimension offset):
+//   byte(m, k) = (k / 8) * (R * 16) + (m / 8) * 128 + (k % 8) * 16 + (m % 8) * 2.
+// Note byte(m, k) of an MN-major tile with R rows equals byte(k, m) of a K-major
+// tile with Kc = R: a row-major [k][m] matrix stored as a K-major tile is, read
+// with this descriptor, its own transpose.
+__host__ __device__ __forceinline__ uint32_t mn_off(int m, int k, int R) {
+  return (uint32_t)((k >> 3) * (R * 16) + (m >> 3) * 128 + (k & 7) * 16 + (m & 7) * 2);
+}
+__device__ __forceinline__ uint64_t mn_desc(uint32_t tile_addr, int R, int kk) {
+  return smem_desc(tile_addr + (uint32_t)kk * 2u * (uint32_t)(R * 16), (uint32_t)(R * 16), 128u);
+}
+// Instruction-descriptor bits selecting MN-major A or B.
+constexpr uint32_t kTransA = 1u << 15;
+constexpr uint32_t kTransB = 1u << 16;
+
 // Instruction descriptor, kind::f16: BF16 A and B (both K-major), float32 D,
 // dense, no negation; N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
@@ -110,6 +128,55 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity,
   return true;
 }
 
+// ---- bulk (TMA, 1-D) and 16-byte asynchronous copies ----------------------
+// Arm the mbarrier for `bytes` of incoming bulk copies (plus one arrival).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_u32(mbar)), "r"(bytes) : "memory");
+}
+// Global -> shared bulk copy; completion is signalled on the mbarrier.
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(mbar)) : "memory");
+}
+// Shared -> global bulk copy (bulk-group completion). Addresses 16-byte
+// aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(gmem_dst), "r"(smem_u32(smem_src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until this thread's committed bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// 16-byte global -> shared copy; src_bytes = 0 fills the destination with zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src,
+                                           uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               :: "r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N committed groups of this thread are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // ---- fences -----------------------------------------------------------------
 __device__ __forceinline__ void fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -140,6 +207,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
       : "r"(taddr) : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr) : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
