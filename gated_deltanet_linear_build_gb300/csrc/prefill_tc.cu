@@ -68,6 +68,15 @@ __host__ __device__ inline TcLayout tc_layout(int T, int N, int Hv) {
 }
 
 // 8 floats -> BF16 hi and lo parts (hi = bf16(x), lo = bf16(x - hi)) as 16-byte vectors.
+// 2^x for x <= 0 (decay ratios), with the hardware base-2 exponential
+// (ex2.approx.ftz: relative error ~2^-22; results below the normal range
+// flush to zero).
+__device__ __forceinline__ float exp2_nonpos(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(fminf(x, 0.f)));
+  return y;
+}
+
 __device__ __forceinline__ void split8(const float* f, uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
 #pragma unroll
@@ -247,7 +256,7 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
                kk > 0);
     mma_commit(mbar);
   }
-  if (tid < 64) cw[tid] = bs[tid] * exp2f(gs[tid]) * rk[tid];
+  if (tid < 64) cw[tid] = bs[tid] * exp2_nonpos(gs[tid]) * rk[tid];
   if (!mbar_wait(mbar, 0)) atomicExch(s_fail, 1);
   fence_after_sync();
   {
@@ -261,12 +270,21 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 #pragma unroll 1
     for (int cb = 0; cb < 8; ++cb) {
       float gv[8], v8[8];
+      // gates and norms of the 8 columns as vector loads, so the 8 entries
+      // below are independent chains
+      const float4 g0 = *reinterpret_cast<const float4*>(gs + 8 * cb);
+      const float4 g1 = *reinterpret_cast<const float4*>(gs + 8 * cb + 4);
+      const float4 k0 = *reinterpret_cast<const float4*>(rk + 8 * cb);
+      const float4 k1 = *reinterpret_cast<const float4*>(rk + 8 * cb + 4);
+      const float gsv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float rkv[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
       tmem_ld8(tmem_warp_addr(taddr, 8 * cb), gv);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int s2 = 8 * cb + e;
         const bool keep = (is_a ? s2 < r : s2 <= r) && r < n;
-        v8[e] = keep ? fr * exp2f(gr - gs[s2]) * rk[s2] * gv[e] : 0.f;
+        const float val = fr * exp2_nonpos(gr - gsv[e]) * rkv[e] * gv[e];
+        v8[e] = keep ? val : 0.f;
       }
       if (is_a) {
         *reinterpret_cast<float4*>(Af + r * 68 + 8 * cb) = make_float4(v8[0], v8[1], v8[2], v8[3]);
@@ -613,11 +631,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (!mbar_wait(tbA, par)) atomicExch(s_fail, 1);
     if (tid == 0) pend_a = -1;
     const float glast = gk[n - 1];
-    const float gamma_c = exp2f(glast);
+    const float gamma_c = exp2_nonpos(glast);
     if (tid < 64) {
       const bool in = tid < n;
-      dks[tid] = in ? exp2f(glast - gk[tid]) * gk[64 + tid] : 0.f;
-      qs[64 * par + tid] = in ? exp2f(gk[tid]) * gk[128 + tid] : 0.f;
+      dks[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
+      qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
     }
     // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
 #pragma unroll
