@@ -515,10 +515,15 @@ def run_gdn(args):
         wl.sweep()                      # eager warm run (sets kernel attributes)
     torch.cuda.synchronize()
     launches_before = wl.stack.launches
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()      # the timed sweep: kernels only
     with torch.cuda.graph(graph, stream=stream):
-        wl.sweep(timer)
+        wl.sweep()
     launches_per_sweep = wl.stack.launches - launches_before
+    tgraph = None                       # the same sweep with event nodes per call
+    if timer is not None:
+        tgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tgraph, stream=stream):
+            wl.sweep(timer)
 
     for _ in range(args.warmup):
         graph.replay()
@@ -529,8 +534,9 @@ def run_gdn(args):
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        for i in range(args.steps):
+            # the last timed sweep is the instrumented one (per-kernel durations)
+            (tgraph if (tgraph is not None and i == args.steps - 1) else graph).replay()
         end.record(stream)
         torch.cuda.synchronize()
     if dist is not None:
@@ -563,8 +569,9 @@ def run_gdn(args):
                    "prefill_steps": len(wl.steps), "step_tokens": STEP_TOKENS,
                    "conv_channels": C, "v_heads": HV, "qk_heads": HK, "head_dim": D,
                    "l2": "inputs larger than L2 (about 11 GB of distinct layer inputs per sweep)",
-                   "timing": "CUDA graph of one sweep, replayed; CUDA events on its stream; "
-                             "per-kernel times from event nodes of the last replay",
+                   "timing": "CUDA graph of one sweep (kernels only) replayed K-1 times, then "
+                             "once the same sweep with event nodes around every call (per-kernel "
+                             "times); CUDA events on the stream bracket all K",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roofline,
         "kernels": kernels,

@@ -8,12 +8,12 @@
 // vLLM", Existing evidence (K=4 specialisation of the conv).
 //
 // GB300 mapping: the conv is HBM-bound (2 bytes in and 2 bytes out per element,
-// 9 flops). One thread owns 8 channels (one 16-byte vector) of one descriptor,
-// keeps the 4 taps of its channels and the 3-token window in registers, issues
-// all of the descriptor's row loads before computing, and writes 16-byte
-// vectors. A CTA covers 1024 channels of one descriptor; with 8-token
-// descriptors the whole 2048 x 8192 prefill is 2048 CTAs, one resident wave on
-// 152 SMs.
+// 9 flops). In the prefill one thread owns 4 channels (an 8-byte vector) of one
+// descriptor, keeps its taps and the 3-token window packed in registers,
+// issues all of the descriptor's row loads before computing, and writes 8-byte
+// vectors; a CTA covers 512 channels of one descriptor, so the 2048 x 8192
+// prefill is 4096 small CTAs, about two resident waves on 152 SMs. The decode
+// update keeps one thread per 8 channels.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -173,6 +173,20 @@ __device__ __forceinline__ void store_state8(__nv_bfloat16* p, const float (&st)
   for (int q = 0; q < 3; ++q) sp[q] = make_uint4(wd[4 * q], wd[4 * q + 1], wd[4 * q + 2], wd[4 * q + 3]);
 }
 
+// Element c (0..3) of 4 BF16 values packed in an 8-byte vector, as float.
+__device__ __forceinline__ float elt4(const uint2& u, int c) {
+  const uint32_t w = c < 2 ? u.x : u.y;
+  return (c & 1) ? bf16hi(w) : bf16lo(w);
+}
+
+__device__ __forceinline__ uint2 ldg8(const void* p) {
+  return __ldg(reinterpret_cast<const uint2*>(p));
+}
+
+// Prefill: one thread owns 4 channels (8-byte vectors) of one unit. The taps
+// (4 channels x 4 taps, two 16-byte vectors), bias and the 3-token window stay
+// packed as BF16 and are converted on use, so a thread needs few registers
+// while it keeps all of a descriptor's rows in flight.
 template <bool kChunks>
 __global__ void __launch_bounds__(kConvThreads)
 conv_fwd_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
@@ -191,36 +205,37 @@ conv_fwd_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
     seq = unit; tok0 = __ldg(cu + unit); len = __ldg(cu + unit + 1) - tok0; pos = 0;
   }
   if (seq < 0 || seq >= N || len <= 0 || pos < 0 || tok0 < pos || (int64_t)tok0 + len > T) return;
-  const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 8;
+  const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 4;
   if (c0 >= C) return;
 
-  float wf[4][8], bf[8];
-  load_taps(w, c0, wf);
-  if (bias) {
-    unpack8(ldg16(bias + c0), bf);
-  } else {
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) bf[ch] = 0.f;
-  }
+  // w[c0 .. c0+3][0..3]: 32 contiguous bytes.
+  const uint4 w01 = ldg16(w + (size_t)c0 * 4), w23 = ldg16(w + (size_t)c0 * 4 + 8);
+  auto tap = [&](int c, int j) {
+    const uint4& u = c < 2 ? w01 : w23;
+    const uint32_t wd = (c & 1) ? (j < 2 ? u.z : u.w) : (j < 2 ? u.x : u.y);
+    return (j & 1) ? bf16hi(wd) : bf16lo(wd);
+  };
+  const uint2 bq = bias ? ldg8(bias + c0) : make_uint2(0, 0);
 
   // Window of the 3 tokens before the unit: slot j holds sequence position
   // pos - 3 + j (from x when >= 0, else from the initial state or zero).
   const bool init = has_init != nullptr && has_init[seq] != 0;
-  __nv_bfloat16* st_row = state + ((size_t)seq * C + c0) * 3;
-  float win[3][8];
-  if (pos < 3) {
-    if (init) {
-      load_state8(st_row, win);
-    } else {
+  __nv_bfloat16* st_row = state + ((size_t)seq * C + c0) * 3;   // 12 BF16: [channel][3]
+  uint2 win[3] = {make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0)};
+  if (pos < 3 && init) {
+    const uint2* sp = reinterpret_cast<const uint2*>(st_row);
+    const uint2 s0 = sp[0], s1 = sp[1], s2 = sp[2];
+    const uint32_t wd[6] = {s0.x, s0.y, s1.x, s1.y, s2.x, s2.y};
+    float sv[3][4];
 #pragma unroll
-      for (int j = 0; j < 3; ++j)
+    for (int e = 0; e < 12; ++e) sv[e % 3][e / 3] = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) win[j][ch] = 0.f;
-    }
+    for (int j = 0; j < 3; ++j)
+      win[j] = make_uint2(pack_bf16x2(sv[j][0], sv[j][1]), pack_bf16x2(sv[j][2], sv[j][3]));
   }
 #pragma unroll
   for (int j = 0; j < 3; ++j) {
-    if (pos - 3 + j >= 0) unpack8(ldg16(x + (size_t)(tok0 - 3 + j) * x_stride + c0), win[j]);
+    if (pos - 3 + j >= 0) win[j] = ldg8(x + (size_t)(tok0 - 3 + j) * x_stride + c0);
   }
 
   // The unit that starts the sequence is the only reader of the old state, so
@@ -228,47 +243,46 @@ conv_fwd_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
   if (pos == 0) {
     const int L = kChunks ? (__ldg(cu + seq + 1) - __ldg(cu + seq)) : len;
     if (L < len || (int64_t)tok0 + L > T) return;  // descriptors inconsistent with cu_seqlens
-    float ns[3][8];
+    uint2 ns[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       const int p = L - 3 + j;
-      if (p >= 0) {
-        unpack8(ldg16(x + (size_t)(tok0 + p) * x_stride + c0), ns[j]);
-      } else {
-        // p in {-3, -2, -1}: old state slot p + 3 (selected without dynamic
-        // register-array indexing).
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          ns[j][ch] = (p == -3) ? win[0][ch] : ((p == -2) ? win[1][ch] : win[2][ch]);
-      }
+      ns[j] = p >= 0 ? ldg8(x + (size_t)(tok0 + p) * x_stride + c0)
+                     : ((p == -3) ? win[0] : ((p == -2) ? win[1] : win[2]));
     }
-    store_state8(st_row, ns);
+    float nv[12];
+#pragma unroll
+    for (int e = 0; e < 12; ++e) nv[e] = elt4(ns[e % 3], e / 3);   // [channel][3] order
+    uint2* sp = reinterpret_cast<uint2*>(st_row);
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+      sp[q] = make_uint2(pack_bf16x2(nv[4 * q], nv[4 * q + 1]), pack_bf16x2(nv[4 * q + 2], nv[4 * q + 3]));
   }
 
   for (int base = 0; base < len; base += 8) {
     const int cnt = min(8, len - base);
-    uint4 xr[8];
+    uint2 xr[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (i < cnt) xr[i] = ldg16(x + (size_t)(tok0 + base + i) * x_stride + c0);
+      if (i < cnt) xr[i] = ldg8(x + (size_t)(tok0 + base + i) * x_stride + c0);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       if (i < cnt) {
-        float xc[8], out[8];
-        unpack8(xr[i], xc);
+        float out[4];
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float acc = bf[ch];
-          acc = fmaf(wf[0][ch], win[0][ch], acc);
-          acc = fmaf(wf[1][ch], win[1][ch], acc);
-          acc = fmaf(wf[2][ch], win[2][ch], acc);
-          acc = fmaf(wf[3][ch], xc[ch], acc);
+        for (int ch = 0; ch < 4; ++ch) {
+          float acc = elt4(bq, ch);
+          acc = fmaf(tap(ch, 0), elt4(win[0], ch), acc);
+          acc = fmaf(tap(ch, 1), elt4(win[1], ch), acc);
+          acc = fmaf(tap(ch, 2), elt4(win[2], ch), acc);
+          acc = fmaf(tap(ch, 3), elt4(xr[i], ch), acc);
           out[ch] = silu ? silu_f(acc) : acc;
-          win[0][ch] = win[1][ch];
-          win[1][ch] = win[2][ch];
-          win[2][ch] = xc[ch];
         }
-        *reinterpret_cast<uint4*>(y + (size_t)(tok0 + base + i) * C + c0) = pack8(out);
+        win[0] = win[1];
+        win[1] = win[2];
+        win[2] = xr[i];
+        *reinterpret_cast<uint2*>(y + (size_t)(tok0 + base + i) * C + c0) =
+            make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
       }
     }
   }
@@ -329,7 +343,7 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
                              int32_t units, int32_t T, int32_t C, int32_t N, int32_t silu,
                              void* y, cudaStream_t st) {
   if (units <= 0) return GDN_OK;
-  dim3 grid(units, (C / 8 + kConvThreads - 1) / kConvThreads);
+  dim3 grid(units, (C / 4 + kConvThreads - 1) / kConvThreads);
   auto xp = static_cast<const __nv_bfloat16*>(x);
   auto wp = static_cast<const __nv_bfloat16*>(w);
   auto bp = static_cast<const __nv_bfloat16*>(bias);
