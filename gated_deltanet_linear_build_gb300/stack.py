@@ -77,12 +77,14 @@ class GdnLayerStack:
     Shapes follow the Qwen3.5-4B-style layer: conv over C = 2*Hk*d + Hv*d
     channels (q | k | v), Hk q/k heads and Hv v-heads of width d.
     Per layer: conv weights [C, 4] BF16, conv_state [n_seqs, C, 3] BF16 and
-    S [n_seqs, Hv, d, d] float32.
+    S [n_seqs, Hv, d, d] float32. The conv weights are drawn N(0, w_std^2)
+    from ``seed`` unless ``conv_weights`` (one [C, 4] tensor per layer) is
+    given.
     """
 
     def __init__(self, layers: int, n_seqs: int, *, hk: int = 16, hv: int = 32, d: int = 128,
                  max_step_tokens: int = 2048, device="cuda", seed: int = 0,
-                 w_std: float = 0.5):
+                 w_std: float = 0.5, conv_weights=None):
         self.layers, self.n_seqs = layers, n_seqs
         self.hk, self.hv, self.d = hk, hv, d
         self.C = 2 * hk * d + hv * d
@@ -90,8 +92,14 @@ class GdnLayerStack:
         g = torch.Generator(device=self.device)
         g.manual_seed(seed)
         C = self.C
-        self.w = [(torch.randn((C, 4), generator=g, device=self.device) * w_std).to(torch.bfloat16)
-                  for _ in range(layers)]
+        if conv_weights is not None:
+            assert len(conv_weights) == layers
+            self.w = [w.to(device=self.device, dtype=torch.bfloat16).contiguous()
+                      for w in conv_weights]
+            assert all(tuple(w.shape) == (C, 4) for w in self.w)
+        else:
+            self.w = [(torch.randn((C, 4), generator=g, device=self.device) * w_std)
+                      .to(torch.bfloat16) for _ in range(layers)]
         self.conv_state = [torch.zeros((n_seqs, C, 3), dtype=torch.bfloat16, device=self.device)
                            for _ in range(layers)]
         self.S = [torch.zeros((n_seqs, hv, d, d), dtype=torch.float32, device=self.device)
@@ -123,6 +131,42 @@ class GdnLayerStack:
         assert slots == list(range(slots[0], slots[0] + len(slots))), "slots are contiguous"
         return cu, has, slots[0]
 
+    # -- one call per kernel family -------------------------------------------
+    def build_chunks(self, cu_d):
+        """Exact 8-token conv descriptors of one prefill step (built once per step)."""
+        gdn.build_conv_chunks(cu_d, self.chunks, self.num_chunks, chunk_tokens=8)
+        self.launches += 1
+
+    def prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, x, a, b, y, out,
+                      tick=None):
+        """Layer l of a prefill step: conv prefill over the step's descriptors,
+        then the chunked delta rule on q/k/v read in place from the conv output."""
+        tick = tick if tick is not None else (lambda kind, edge: None)
+        sl = slice(first_slot, first_slot + n)
+        tick("conv_prefill", "start")
+        gdn.causal_conv1d_fwd(x, self.w[l], None, self.conv_state[l][sl], has_d, cu_d, y,
+                              chunks=self.chunks, num_chunks=self.num_chunks)
+        tick("conv_prefill", "end")
+        q, k, v = self.qkv(y)
+        tick("delta_prefill", "start")
+        gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, out,
+                                       self.workspace, qk_l2norm=True)
+        tick("delta_prefill", "end")
+        self.launches += 1 + PREFILL_LAUNCHES
+
+    def decode_layer(self, l: int, x, a, b, y, out, tick=None):
+        """Layer l of a decode step: conv update, then the delta-rule decode."""
+        tick = tick if tick is not None else (lambda kind, edge: None)
+        tick("conv_update", "start")
+        gdn.causal_conv1d_update(x, self.w[l], None, self.conv_state[l], y)
+        tick("conv_update", "end")
+        q, k, v = self.qkv(y)
+        tick("delta_decode", "start")
+        gdn.delta_rule_decode(q, k, v, a, b, self.S[l], out, qk_l2norm=True)
+        tick("delta_decode", "end")
+        self.launches += 2
+
+    # -- whole engine steps over precomputed layer inputs ------------------------
     def prefill_step(self, cu_d, has_d, first_slot: int, n: int, xs, gates, ys, outs,
                      timer=None):
         """One prefill engine step over all layers.
@@ -134,34 +178,14 @@ class GdnLayerStack:
         """
         tick = timer if timer is not None else (lambda kind, edge: None)
         tick("build_chunks", "start")
-        gdn.build_conv_chunks(cu_d, self.chunks, self.num_chunks, chunk_tokens=8)
+        self.build_chunks(cu_d)
         tick("build_chunks", "end")
-        self.launches += 1
-        sl = slice(first_slot, first_slot + n)
         for l in range(self.layers):
-            x, y = xs[l], ys[l]
-            tick("conv_prefill", "start")
-            gdn.causal_conv1d_fwd(x, self.w[l], None, self.conv_state[l][sl], has_d, cu_d, y,
-                                  chunks=self.chunks, num_chunks=self.num_chunks)
-            tick("conv_prefill", "end")
-            q, k, v = self.qkv(y)
             a, b = gates[l]
-            tick("delta_prefill", "start")
-            gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, outs[l],
-                                           self.workspace, qk_l2norm=True)
-            tick("delta_prefill", "end")
-            self.launches += 1 + PREFILL_LAUNCHES
+            self.prefill_layer(l, cu_d, has_d, first_slot, n, xs[l], a, b, ys[l], outs[l], tick)
 
     def decode_step(self, xs, gates, ys, outs, timer=None):
         """One decode engine step (one token for every slot) over all layers."""
-        tick = timer if timer is not None else (lambda kind, edge: None)
         for l in range(self.layers):
-            tick("conv_update", "start")
-            gdn.causal_conv1d_update(xs[l], self.w[l], None, self.conv_state[l], ys[l])
-            tick("conv_update", "end")
-            q, k, v = self.qkv(ys[l])
             a, b = gates[l]
-            tick("delta_decode", "start")
-            gdn.delta_rule_decode(q, k, v, a, b, self.S[l], outs[l], qk_l2norm=True)
-            tick("delta_decode", "end")
-            self.launches += 2
+            self.decode_layer(l, xs[l], a, b, ys[l], outs[l], timer)

@@ -200,3 +200,32 @@ def serving_mix_lengths(seed: int = 4, n: int = SERVING_SEQS, lo: int = 512, hi:
     """Prompt lengths of the serving mix: n integers uniform on [lo, hi]."""
     rng = np.random.default_rng(seed)
     return rng.integers(lo, hi + 1, size=n).astype(np.int64)
+
+
+SERVING_VOCAB = 4096
+
+
+def serving_stack(seed: int = 4, layers: int = SERVING_LAYERS, n_seqs: int = SERVING_SEQS,
+                  vocab: int = SERVING_VOCAB, hk: int = QK_HEADS, hv: int = V_HEADS,
+                  d: int = HEAD_DIM, len_lo: int = 512, len_hi: int = 1024):
+    """Weights and prompts of the synthetic GDN stack used by the serving mix.
+
+    embed [vocab, C] BF16 ~ N(0,1); per layer: conv taps [C, 4] BF16 ~ N(0, 0.5^2),
+    gate projections u, r [hv, d] float32 ~ N(0,1), residual scales [C] float32 ~
+    N(0, 0.5^2); head [C, vocab] BF16 ~ N(0, 1/C); prompts: lengths U[len_lo,
+    len_hi] (seed ``seed``) and token ids U[0, vocab) (seed ``seed + 1000``).
+    """
+    C = 2 * hk * d + hv * d
+    rng = np.random.default_rng(seed + 500)
+    embed = normal_bf16(rng, (vocab, C))
+    conv_w = [normal_bf16(rng, (C, CONV_K), std=0.5) for _ in range(layers)]
+    gate_u = [rng.standard_normal((hv, d)).astype(np.float32) for _ in range(layers)]
+    gate_r = [rng.standard_normal((hv, d)).astype(np.float32) for _ in range(layers)]
+    res_scale = [(0.5 * rng.standard_normal(C)).astype(np.float32) for _ in range(layers)]
+    head = normal_bf16(rng, (C, vocab), std=1.0 / np.sqrt(C))
+    lengths = [int(x) for x in serving_mix_lengths(seed, n_seqs, len_lo, len_hi)]
+    ids_rng = np.random.default_rng(seed + 1000)
+    prompts = [ids_rng.integers(0, vocab, size=L).astype(np.int64) for L in lengths]
+    return dict(embed=embed, conv_w=conv_w, gate_u=gate_u, gate_r=gate_r, res_scale=res_scale,
+                head=head, prompts=prompts, lengths=lengths, layers=layers, hk=hk, hv=hv, d=d,
+                C=C, vocab=vocab)

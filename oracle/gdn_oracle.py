@@ -367,3 +367,116 @@ def rel_err(x, ref) -> float:
     if den == 0.0:
         return float(num)
     return float(num / den)
+
+
+# ----------------------------------------------------------------------------
+# The synthetic GDN stack of the serving mix (greedy generation, one sequence)
+# ----------------------------------------------------------------------------
+#
+# Readings (the pages name the model -- a Qwen3.5-style hybrid -- but give no
+# definition of a synthetic stack): a residual stream h (float32 storage); per
+# layer x = bf16(h / sqrt(mean(h^2) + 1e-6)); the conv over x (BF16 output);
+# q, k, v split from it, q and k L2-normalised inside the delta rule; gates
+# a = exp(-softplus(u_h . x_v[h] / sqrt(d))) and b = sigmoid(r_h . x_v[h] /
+# sqrt(d)) from the pre-conv v slice of head h, stored as float32; the delta
+# rule's BF16 output o; h <- h + s * [o, o] (the 4096-wide output repeated to
+# the 8192-wide stream). Head: logits = bf16(rms-normalised h) . W, argmax
+# with the lowest index winning ties. The first generated token comes from the
+# last prompt position; each decode step consumes the previous token.
+
+RMS_EPS = 1e-6
+
+
+def rms_norm_bf16(h):
+    """BF16 bit patterns of h / sqrt(mean(h^2) + 1e-6), row by row."""
+    h = np.asarray(h, np.float64)
+    return to_bf16(h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + RMS_EPS))
+
+
+def _gates(x_vals, u, r, hk, hv, d):
+    xv = x_vals[:, 2 * hk * d:].reshape(-1, hv, d)
+    za = np.einsum("lhd,hd->lh", xv, np.asarray(u, np.float64)) / np.sqrt(d)
+    zb = np.einsum("lhd,hd->lh", xv, np.asarray(r, np.float64)) / np.sqrt(d)
+    a = np.exp(-np.logaddexp(0.0, za)).astype(np.float32)
+    b = (1.0 / (1.0 + np.exp(-zb))).astype(np.float32)
+    return a, b
+
+
+def _stack_layer(stack, l, h, carry, first: bool, chunk: int):
+    """Layer l of the synthetic stack on rows h [T, C] of ONE sequence.
+
+    first: the rows are the whole prompt (conv prefill and chunked delta rule
+    from zero state); otherwise h holds one decode token. carry["conv"][l] and
+    carry["S"][l] are read and replaced. Returns the new residual stream rows.
+    """
+    hk, hv, d = stack["hk"], stack["hv"], stack["d"]
+    T = h.shape[0]
+    xb = rms_norm_bf16(h)
+    a, b = _gates(from_bf16(xb), stack["gate_u"][l], stack["gate_r"][l], hk, hv, d)
+    if first:
+        y, st = causal_conv1d_fwd(xb, stack["conv_w"][l], None, carry["conv"][l], [0], [0, T])
+    else:
+        y, st = causal_conv1d_update(xb, stack["conv_w"][l], None, carry["conv"][l])
+    carry["conv"][l] = to_bf16(st)
+    yb = to_bf16(y)
+    q = yb[:, :hk * d].reshape(T, hk, d)
+    k = yb[:, hk * d:2 * hk * d].reshape(T, hk, d)
+    v = yb[:, 2 * hk * d:].reshape(T, hv, d)
+    if first:
+        o, carry["S"][l] = delta_rule_prefill_chunked(q, k, v, a, b, [0, T], carry["S"][l], [0],
+                                                      qk_l2norm=True, chunk=chunk)
+    else:
+        o, carry["S"][l] = delta_rule_decode(q, k, v, a, b, carry["S"][l], qk_l2norm=True)
+    ob = round_bf16(o).reshape(T, hv * d)
+    return h + np.asarray(stack["res_scale"][l], np.float64) * np.concatenate([ob, ob], axis=1)
+
+
+def _new_carry(stack):
+    C, hv, d = stack["C"], stack["hv"], stack["d"]
+    return dict(conv=[np.zeros((1, C, 3), np.uint16) for _ in range(stack["layers"])],
+                S=[np.zeros((1, hv, d, d)) for _ in range(stack["layers"])])
+
+
+def stack_logits(stack, h_rows):
+    """Head logits of residual rows: bf16(rms-normalised h) . W (float64)."""
+    return from_bf16(rms_norm_bf16(h_rows)) @ from_bf16(stack["head"])
+
+
+def serving_stack_sequence(stack, s: int, n_decode: int = 128, chunk: int = 64):
+    """Greedy generation of sequence s through the synthetic stack.
+
+    Prompt: ``stack["prompts"][s]``; returns (ids, margins, logits_rows): the
+    n_decode + 1 generated ids, the top-1 minus top-2 logit margin at each, and
+    the logits rows (float64). The prompt goes through each layer at once
+    (chunked evaluation of the delta rule, pinned equal to the sequential
+    one); decode steps use the single-token forms.
+    """
+    embed = from_bf16(stack["embed"])
+    carry = _new_carry(stack)
+    h = embed[np.asarray(stack["prompts"][s])]
+    for l in range(stack["layers"]):
+        h = _stack_layer(stack, l, h, carry, True, chunk)
+    ids, margins, rows = [], [], []
+    lg = stack_logits(stack, h[-1:])[0]
+    for step in range(n_decode + 1):
+        top = int(np.argmax(lg))       # first index of the maximum
+        srt = np.sort(lg)
+        ids.append(top)
+        margins.append(float(srt[-1] - srt[-2]))
+        rows.append(lg)
+        if step == n_decode:
+            break
+        h = embed[[top]]
+        for l in range(stack["layers"]):
+            h = _stack_layer(stack, l, h, carry, False, chunk)
+        lg = stack_logits(stack, h)[0]
+    return ids, margins, np.asarray(rows)
+
+
+def serving_stack_prefill_logits(stack, tokens, chunk: int = 64):
+    """Logits at every position of ``tokens`` run through the stack as one prompt."""
+    carry = _new_carry(stack)
+    h = from_bf16(stack["embed"])[np.asarray(tokens)]
+    for l in range(stack["layers"]):
+        h = _stack_layer(stack, l, h, carry, True, chunk)
+    return stack_logits(stack, h)
