@@ -8,13 +8,17 @@
 // vLLM", Existing evidence (K=4 specialisation of the conv).
 //
 // GB300 mapping: the conv is HBM-bound (2 bytes in and 2 bytes out per element,
-// 9 flops). In the prefill one thread owns 4 channels (an 8-byte vector) of one
-// descriptor, keeps its taps and the 3-token window packed in registers,
-// issues all of the descriptor's row loads before computing, and writes 8-byte
-// vectors; a CTA covers 512 channels of one descriptor, so the 2048 x 8192
-// prefill is 4096 small CTAs, about two resident waves on 152 SMs. The decode
-// update keeps one thread per 8 channels.
+// 9 flops and one SiLU). The prefill is a persistent stream: one CTA per SM
+// walks a contiguous run of descriptors for one 2048-channel block, a producer
+// warp keeps up to 192 KB of token rows in flight with bulk copies into a ring
+// of shared-memory stages, and the compute warps convolve each stage from
+// shared memory (the window of a continuing descriptor stays in registers).
+// The whole-sequence mapping is the same kernel with one descriptor per
+// sequence. The decode update keeps one thread per 8 channels.
+#include <algorithm>
+
 #include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -173,118 +177,351 @@ __device__ __forceinline__ void store_state8(__nv_bfloat16* p, const float (&st)
   for (int q = 0; q < 3; ++q) sp[q] = make_uint4(wd[4 * q], wd[4 * q + 1], wd[4 * q + 2], wd[4 * q + 3]);
 }
 
-// Element c (0..3) of 4 BF16 values packed in an 8-byte vector, as float.
-__device__ __forceinline__ float elt4(const uint2& u, int c) {
-  const uint32_t w = c < 2 ? u.x : u.y;
-  return (c & 1) ? bf16hi(w) : bf16lo(w);
+// Prefill stream kernel. One CTA per SM: kCvGroups producer warps and
+// kCvGroups groups of compute warps. The grid is NB channel blocks (kCvChan
+// channels each) x R token groups; the CTA of (block cb, group r) owns
+// descriptors [n r / R, n (r + 1) / R) of channel block cb. Every producer
+// warp reads the CTA's descriptors up front (one per lane) and walks the same
+// list of stages, kCvRows tokens each; stage i is posted by producer warp
+// i % kCvGroups into slot i % kCvStages of a shared-memory ring, with bulk
+// copies of the stage's rows, its 3-token halo (the 3 rows before it, or the
+// initial conv_state at the start of a sequence) and, on the first stage of a
+// sequence longer than the stage, the sequence's last 3 rows (the new
+// conv_state). Several posting warps are needed because each mbarrier phase
+// costs a posting thread a fixed time of the order of a few 2 KB copies. Every
+// stage is self-contained, and stage i goes to compute group i % kCvGroups: a
+// thread convolves 8 channels from shared memory (taps in registers, 16-byte
+// loads and stores) and the group hands the stage back. No compute warp
+// touches global memory except to store y and the new conv_state, so no load
+// latency sits on the compute path.
+constexpr int kCvGroups = 3;
+constexpr int kCvGroupWarps = 8;
+constexpr int kCvCpt = 4;                                // channels per compute thread
+constexpr int kCvComputeWarps = kCvGroups * kCvGroupWarps;
+constexpr int kCvThreads = (kCvComputeWarps + kCvGroups) * 32;   // + producer warps
+constexpr int kCvChan = kCvGroupWarps * 32 * kCvCpt;     // 1024 channels per CTA
+constexpr int kCvRows = 8;                               // tokens per stage
+constexpr int kCvSlot = kCvChan * 2;                     // one token's row segment (bytes)
+constexpr int kCvHalo = 0, kCvData = 3, kCvTail = 3 + kCvRows;   // slot indices
+constexpr int kCvStageBytes = (3 + kCvRows + 3) * kCvSlot;        // 28 KB
+constexpr int kCvStages = 7;
+constexpr int kCvMetaOff = kCvStages * kCvStageBytes;
+constexpr int kCvBarOff = kCvMetaOff + kCvStages * 32;
+constexpr int kCvSmem = kCvBarOff + 2 * kCvStages * 8;
+// Stage flags.
+constexpr int kHaloX = 1;        // halo slots hold x rows tok-3 .. tok-1
+constexpr int kHaloState = 2;    // halo slots hold the initial conv_state [ch][3]
+constexpr int kFirst = 4;        // first stage of a sequence: writes the new conv_state
+constexpr int kTailRows = 8;     // tail slots hold the sequence's last 3 rows
+
+// One token of 4 channels (2 pairs): y = act(bias + w0 x[-3] + w1 x[-2] +
+// w2 x[-1] + w3 x[0]) with the window win = (x[-3], x[-2], x[-1]), which then
+// shifts by one. The products accumulate in this order in float32.
+template <bool kSilu>
+__device__ __forceinline__ void conv_row(const uint2 u, __nv_bfloat16* yd,
+                                         const float2 (&wf)[4][2], const float2 (&bf)[2],
+                                         float2 (&win)[3][2]) {
+  const uint32_t xw[2] = {u.x, u.y};
+  uint32_t ow[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float2 xc = bf16x2_f2(xw[q]);
+    float2 acc = fma2(wf[0][q], win[0][q], bf[q]);
+    acc = fma2(wf[1][q], win[1][q], acc);
+    acc = fma2(wf[2][q], win[2][q], acc);
+    acc = fma2(wf[3][q], xc, acc);
+    ow[q] = f2_bf16x2(kSilu ? silu2(acc) : acc);
+    win[0][q] = win[1][q];
+    win[1][q] = win[2][q];
+    win[2][q] = xc;
+  }
+  *reinterpret_cast<uint2*>(yd) = make_uint2(ow[0], ow[1]);
 }
 
-__device__ __forceinline__ uint2 ldg8(const void* p) {
-  return __ldg(reinterpret_cast<const uint2*>(p));
+// conv_state of 4 channels ([channel][3], 24 bytes, 8-byte aligned) <-> floats.
+__device__ __forceinline__ void state4_from_words(const uint2 (&u)[3], float (&st)[3][4]) {
+  const uint32_t wd[6] = {u[0].x, u[0].y, u[1].x, u[1].y, u[2].x, u[2].y};
+#pragma unroll
+  for (int e = 0; e < 12; ++e) {
+    const uint32_t word = wd[e >> 1];
+    st[e % 3][e / 3] = (e & 1) ? bf16hi(word) : bf16lo(word);
+  }
+}
+__device__ __forceinline__ void store_state4(__nv_bfloat16* p, const float (&st)[3][4]) {
+  uint32_t wd[6];
+#pragma unroll
+  for (int e = 0; e < 12; e += 2)
+    wd[e >> 1] = pack_bf16x2(st[e % 3][e / 3], st[(e + 1) % 3][(e + 1) / 3]);
+  uint2* sp = reinterpret_cast<uint2*>(p);
+#pragma unroll
+  for (int q = 0; q < 3; ++q) sp[q] = make_uint2(wd[2 * q], wd[2 * q + 1]);
+}
+// a[i][ch] for a runtime i in 0..2, without indexing a register array.
+__device__ __forceinline__ float sel3_4(const float (&a)[3][4], int i, int ch) {
+  return i == 0 ? a[0][ch] : (i == 1 ? a[1][ch] : a[2][ch]);
 }
 
-// Prefill: one thread owns 4 channels (8-byte vectors) of one unit. The taps
-// (4 channels x 4 taps, two 16-byte vectors), bias and the 3-token window stay
-// packed as BF16 and are converted on use, so a thread needs few registers
-// while it keeps all of a descriptor's rows in flight.
-template <bool kChunks>
-__global__ void __launch_bounds__(kConvThreads)
-conv_fwd_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
-                const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ bias,
-                __nv_bfloat16* __restrict__ state, const uint8_t* __restrict__ has_init,
-                const int32_t* __restrict__ cu, const gdn_conv_chunk_t* __restrict__ chunks,
-                const int32_t* __restrict__ num_chunks, int T, int C, int N, int silu,
-                __nv_bfloat16* __restrict__ y) {
-  const int unit = blockIdx.x;
-  int seq, tok0, len, pos;
-  if (kChunks) {
-    if (unit >= __ldg(num_chunks)) return;
-    const int4 d = __ldg(reinterpret_cast<const int4*>(chunks) + unit);
-    seq = d.x; tok0 = d.y; len = d.z; pos = d.w;
-  } else {
-    seq = unit; tok0 = __ldg(cu + unit); len = __ldg(cu + unit + 1) - tok0; pos = 0;
-  }
-  if (seq < 0 || seq >= N || len <= 0 || pos < 0 || tok0 < pos || (int64_t)tok0 + len > T) return;
-  const int c0 = (blockIdx.y * kConvThreads + threadIdx.x) * 4;
-  if (c0 >= C) return;
+struct CvMeta {
+  int seq, tok, rows, pos, flags, L;
+};
 
-  // w[c0 .. c0+3][0..3]: 32 contiguous bytes.
-  const uint4 w01 = ldg16(w + (size_t)c0 * 4), w23 = ldg16(w + (size_t)c0 * 4 + 8);
-  auto tap = [&](int c, int j) {
-    const uint4& u = c < 2 ? w01 : w23;
-    const uint32_t wd = (c & 1) ? (j < 2 ? u.z : u.w) : (j < 2 ? u.x : u.y);
-    return (j & 1) ? bf16hi(wd) : bf16lo(wd);
-  };
-  const uint2 bq = bias ? ldg8(bias + c0) : make_uint2(0, 0);
-
-  // Window of the 3 tokens before the unit: slot j holds sequence position
-  // pos - 3 + j (from x when >= 0, else from the initial state or zero).
-  const bool init = has_init != nullptr && has_init[seq] != 0;
-  __nv_bfloat16* st_row = state + ((size_t)seq * C + c0) * 3;   // 12 BF16: [channel][3]
-  uint2 win[3] = {make_uint2(0, 0), make_uint2(0, 0), make_uint2(0, 0)};
-  if (pos < 3 && init) {
-    const uint2* sp = reinterpret_cast<const uint2*>(st_row);
-    const uint2 s0 = sp[0], s1 = sp[1], s2 = sp[2];
-    const uint32_t wd[6] = {s0.x, s0.y, s1.x, s1.y, s2.x, s2.y};
-    float sv[3][4];
-#pragma unroll
-    for (int e = 0; e < 12; ++e) sv[e % 3][e / 3] = (e & 1) ? bf16hi(wd[e >> 1]) : bf16lo(wd[e >> 1]);
-#pragma unroll
-    for (int j = 0; j < 3; ++j)
-      win[j] = make_uint2(pack_bf16x2(sv[j][0], sv[j][1]), pack_bf16x2(sv[j][2], sv[j][3]));
-  }
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    if (pos - 3 + j >= 0) win[j] = ldg8(x + (size_t)(tok0 - 3 + j) * x_stride + c0);
-  }
-
-  // The unit that starts the sequence is the only reader of the old state, so
-  // it also writes the new one: the last 3 entries of (old state ++ x_seq).
-  if (pos == 0) {
-    const int L = kChunks ? (__ldg(cu + seq + 1) - __ldg(cu + seq)) : len;
-    if (L < len || (int64_t)tok0 + L > T) return;  // descriptors inconsistent with cu_seqlens
-    uint2 ns[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int p = L - 3 + j;
-      ns[j] = p >= 0 ? ldg8(x + (size_t)(tok0 + p) * x_stride + c0)
-                     : ((p == -3) ? win[0] : ((p == -2) ? win[1] : win[2]));
+template <bool kSilu>
+__global__ void __launch_bounds__(kCvThreads, 1)
+conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
+                       const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ bias,
+                       __nv_bfloat16* __restrict__ state, const uint8_t* __restrict__ has_init,
+                       const int32_t* __restrict__ cu, const gdn_conv_chunk_t* __restrict__ chunks,
+                       const int32_t* __restrict__ num_chunks, int units, int T, int C, int N,
+                       __nv_bfloat16* __restrict__ y) {
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char sm[];
+  CvMeta* meta = reinterpret_cast<CvMeta*>(sm + kCvMetaOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kCvBarOff);
+  uint64_t* empty = full + kCvStages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NB = (C + kCvChan - 1) / kCvChan;
+  const int R = gridDim.x / NB;
+  const int cb = blockIdx.x % NB, grp = blockIdx.x / NB;
+  const int c_base = cb * kCvChan;
+  const int nch = min(kCvChan, C - c_base);
+  if (tid == 0) {
+    for (int st = 0; st < kCvStages; ++st) {
+      mbar_init(full + st, 1);
+      mbar_init(empty + st, kCvGroupWarps);
     }
-    float nv[12];
-#pragma unroll
-    for (int e = 0; e < 12; ++e) nv[e] = elt4(ns[e % 3], e / 3);   // [channel][3] order
-    uint2* sp = reinterpret_cast<uint2*>(st_row);
-#pragma unroll
-    for (int q = 0; q < 3; ++q)
-      sp[q] = make_uint2(pack_bf16x2(nv[4 * q], nv[4 * q + 1]), pack_bf16x2(nv[4 * q + 2], nv[4 * q + 3]));
   }
+  __syncthreads();
 
-  for (int base = 0; base < len; base += 8) {
-    const int cnt = min(8, len - base);
-    uint2 xr[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (i < cnt) xr[i] = ldg8(x + (size_t)(tok0 + base + i) * x_stride + c0);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < cnt) {
-        float out[4];
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float acc = elt4(bq, ch);
-          acc = fmaf(tap(ch, 0), elt4(win[0], ch), acc);
-          acc = fmaf(tap(ch, 1), elt4(win[1], ch), acc);
-          acc = fmaf(tap(ch, 2), elt4(win[2], ch), acc);
-          acc = fmaf(tap(ch, 3), elt4(xr[i], ch), acc);
-          out[ch] = silu ? silu_f(acc) : acc;
+  if (warp >= kCvComputeWarps) {
+    // Producer warp pw. Lanes fetch and validate 32 descriptors at a time;
+    // lane 0 posts the stages i with i % kCvGroups == pw, then the end marker
+    // (rows = -1) of compute group pw.
+    const int pw = warp - kCvComputeWarps;
+    // The split over token groups uses the capacity, so the count and the
+    // descriptors load together; entries at or past the count are skipped.
+    const int d0 = (int)(((int64_t)units * grp) / R);
+    const int d1 = (int)(((int64_t)units * (grp + 1)) / R);
+    const uint32_t seg = (uint32_t)nch * 2u;
+    int it = 0;
+    bool ok = true;
+    auto post = [&](const CvMeta& m, uint32_t bytes, int st) {
+      meta[st] = m;
+      if (bytes)
+        mbar_arrive_expect_tx(full + st, bytes);
+      else
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(full + st))
+                     : "memory");
+    };
+    for (int base = d0; base < d1 && ok; base += 32) {
+      const int d = base + lane;
+      int4 dd = make_int4(-1, 0, 0, 0);
+      int L = 0, init = 0;
+      if (d < d1) {
+        int n;
+        if (chunks) {
+          n = __ldg(num_chunks);
+          dd = __ldg(reinterpret_cast<const int4*>(chunks) + d);
+        } else {
+          n = N;
+          const int t0 = __ldg(cu + d);
+          dd = make_int4(d, t0, __ldg(cu + d + 1) - t0, 0);
         }
-        win[0] = win[1];
-        win[1] = win[2];
-        win[2] = xr[i];
-        *reinterpret_cast<uint2*>(y + (size_t)(tok0 + base + i) * C + c0) =
-            make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
+        const int seq = dd.x, tok0 = dd.y, len = dd.z, pos = dd.w;
+        bool valid = d < n && seq >= 0 && seq < N && len > 0 && (pos == 0 || pos >= 3) &&
+                     tok0 >= pos && (int64_t)tok0 + len <= T;
+        if (valid && pos == 0) {
+          // Only the first descriptor of a sequence needs the sequence
+          // length (for the new state) and the initial-state flag.
+          L = __ldg(cu + seq + 1) - __ldg(cu + seq);
+          init = has_init != nullptr && has_init[seq] != 0;
+          // descriptors inconsistent with cu_seqlens are skipped
+          if (L < len || (int64_t)tok0 + L > T) valid = false;
+        }
+        if (!valid) dd.x = -1;
+      }
+      const int cnt = min(32, d1 - base);
+      for (int j = 0; j < cnt; ++j) {
+        const int seq = __shfl_sync(0xffffffffu, dd.x, j);
+        const int tok0 = __shfl_sync(0xffffffffu, dd.y, j);
+        const int len = __shfl_sync(0xffffffffu, dd.z, j);
+        const int pos = __shfl_sync(0xffffffffu, dd.w, j);
+        const int Lj = __shfl_sync(0xffffffffu, L, j);
+        const int initj = __shfl_sync(0xffffffffu, init, j);
+        if (seq < 0) continue;
+        if (lane == 0) {
+          for (int r0 = 0; r0 < len && ok; r0 += kCvRows, ++it) {
+            if (it % kCvGroups != pw) continue;
+            const int st = it % kCvStages;
+            if (it >= kCvStages && !mbar_wait_sleep(empty + st, ((it / kCvStages) - 1) & 1, 128)) {
+              ok = false;
+              break;
+            }
+            CvMeta m;
+            m.seq = seq;
+            m.tok = tok0 + r0;
+            m.rows = min(kCvRows, len - r0);
+            m.pos = pos + r0;
+            m.L = Lj;
+            m.flags = 0;
+            unsigned char* dst = sm + st * kCvStageBytes;
+            const __nv_bfloat16* xr = x + (int64_t)m.tok * x_stride + c_base;
+            uint32_t bytes = (uint32_t)m.rows * seg;
+            if (m.pos >= 3) {
+              m.flags |= kHaloX;
+              bytes += 3 * seg;
+            } else if (initj) {
+              m.flags |= kHaloState;
+              bytes += 3 * seg;
+            }
+            if (m.pos == 0) {
+              m.flags |= kFirst;
+              if (Lj > m.rows) {
+                m.flags |= kTailRows;
+                bytes += 3 * seg;
+              }
+            }
+            post(m, bytes, st);
+            for (int i = 0; i < m.rows; ++i)
+              bulk_g2s(dst + (kCvData + i) * kCvSlot, xr + (int64_t)i * x_stride, seg, full + st);
+            if (m.flags & kHaloX) {
+              for (int i = 0; i < 3; ++i)
+                bulk_g2s(dst + (kCvHalo + i) * kCvSlot, xr - (int64_t)(3 - i) * x_stride, seg,
+                         full + st);
+            } else if (m.flags & kHaloState) {
+              bulk_g2s(dst + kCvHalo * kCvSlot, state + ((size_t)seq * C + c_base) * 3, 3 * seg,
+                       full + st);
+            }
+            if (m.flags & kTailRows) {
+              const __nv_bfloat16* xt = x + (int64_t)(tok0 + Lj - 3) * x_stride + c_base;
+              for (int i = 0; i < 3; ++i)
+                bulk_g2s(dst + (kCvTail + i) * kCvSlot, xt + (int64_t)i * x_stride, seg,
+                         full + st);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        it = __shfl_sync(0xffffffffu, it, 0);
       }
     }
+    if (lane == 0 && ok) {
+      while (it % kCvGroups != pw) ++it;
+      const int st = it % kCvStages;
+      if (it < kCvStages || mbar_wait_sleep(empty + st, ((it / kCvStages) - 1) & 1, 128)) {
+        CvMeta m;
+        m.rows = -1;
+        post(m, 0, st);
+      }
+    }
+    return;
+  }
+
+  // Compute group g = warp / kCvGroupWarps takes stages g, g + kCvGroups, ...
+  const int g = warp / kCvGroupWarps;
+  const int gt = tid - g * kCvGroupWarps * 32;   // 0 .. 255
+  const int c0 = c_base + gt * kCvCpt;
+  const bool active = gt * kCvCpt < nch;
+  float2 wf[4][2], bf[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    bf[q] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) wf[j][q] = make_float2(0.f, 0.f);
+  }
+  if (active) {
+    // w is [C, 4]: 4 channels x 4 taps = 32 contiguous bytes.
+    const uint4 w01 = ldg16(w + (size_t)c0 * 4), w23 = ldg16(w + (size_t)c0 * 4 + 8);
+    const uint32_t tw[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+    // word 2 ch + (j >> 1) holds taps j (even: low half) of channel ch
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t a0 = tw[2 * (2 * q) + (j >> 1)], a1 = tw[2 * (2 * q + 1) + (j >> 1)];
+        wf[j][q] = (j & 1) ? make_float2(bf16hi(a0), bf16hi(a1)) : make_float2(bf16lo(a0), bf16lo(a1));
+      }
+    if (bias) {
+      const uint2 bu = *reinterpret_cast<const uint2*>(bias + c0);
+      bf[0] = bf16x2_f2(bu.x);
+      bf[1] = bf16x2_f2(bu.y);
+    }
+  }
+  for (int it = g;; it += kCvGroups) {
+    const int st = it % kCvStages;
+    // A wait that gives up (the producer stopped) ends the stream.
+    if (!mbar_wait_sleep(full + st, (it / kCvStages) & 1)) break;
+    const CvMeta m = meta[st];
+    if (m.rows < 0) break;
+    const unsigned char* stage = sm + st * kCvStageBytes;
+    if (active) {
+      // Window slot j holds sequence position m.pos - 3 + j: an x row from the
+      // halo slots, else the initial state (slot p + 3) or zero.
+      float2 win[3][2];
+      float sv[3][4];
+      if (m.flags & kHaloState) {
+        const uint2* sp = reinterpret_cast<const uint2*>(stage + kCvHalo * kCvSlot + gt * 24);
+        const uint2 su[3] = {sp[0], sp[1], sp[2]};
+        state4_from_words(su, sv);
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) sv[0][ch] = sv[1][ch] = sv[2][ch] = 0.f;
+      }
+      if (m.flags & kHaloX) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const uint2 u = *reinterpret_cast<const uint2*>(stage + (kCvHalo + j) * kCvSlot + gt * 8);
+          win[j][0] = bf16x2_f2(u.x);
+          win[j][1] = bf16x2_f2(u.y);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) win[j][q] = make_float2(sv[j][2 * q], sv[j][2 * q + 1]);
+      }
+      if (m.flags & kFirst) {
+        // The first stage of a sequence is the only reader of the old state,
+        // so it also writes the new one: the last 3 entries of (old ++ x_seq).
+        float ns[3][4];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int p = m.L - 3 + j;
+          if (p < 0) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) ns[j][ch] = sel3_4(sv, p + 3, ch);
+          } else {
+            const int slot = (m.flags & kTailRows) ? kCvTail + j : kCvData + p;
+            const uint2 u = *reinterpret_cast<const uint2*>(stage + slot * kCvSlot + gt * 8);
+            ns[j][0] = bf16lo(u.x);
+            ns[j][1] = bf16hi(u.x);
+            ns[j][2] = bf16lo(u.y);
+            ns[j][3] = bf16hi(u.y);
+          }
+        }
+        store_state4(state + ((size_t)m.seq * C + c0) * 3, ns);
+      }
+      const unsigned char* src = stage + kCvData * kCvSlot + gt * 8;
+      __nv_bfloat16* dst = y + (int64_t)m.tok * C + c0;
+      if (m.rows == kCvRows) {
+        // Full stage: all rows are read from shared memory before the first
+        // store (so no load waits behind a store), then straight-line code
+        // in which the window shifts by renaming.
+        uint2 xr[kCvRows];
+#pragma unroll
+        for (int i = 0; i < kCvRows; ++i)
+          xr[i] = *reinterpret_cast<const uint2*>(src + i * kCvSlot);
+#pragma unroll
+        for (int i = 0; i < kCvRows; ++i)
+          conv_row<kSilu>(xr[i], dst + (int64_t)i * C, wf, bf, win);
+      } else {
+        for (int i = 0; i < m.rows; ++i)
+          conv_row<kSilu>(*reinterpret_cast<const uint2*>(src + i * kCvSlot),
+                          dst + (int64_t)i * C, wf, bf, win);
+      }
+    }
+    __syncwarp();
+    if (lane == 0)
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(empty + st))
+                   : "memory");
   }
 }
 
@@ -343,18 +580,23 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
                              int32_t units, int32_t T, int32_t C, int32_t N, int32_t silu,
                              void* y, cudaStream_t st) {
   if (units <= 0) return GDN_OK;
-  dim3 grid(units, (C / 4 + kConvThreads - 1) / kConvThreads);
-  auto xp = static_cast<const __nv_bfloat16*>(x);
-  auto wp = static_cast<const __nv_bfloat16*>(w);
-  auto bp = static_cast<const __nv_bfloat16*>(bias);
-  auto sp = static_cast<__nv_bfloat16*>(conv_state);
-  auto yp = static_cast<__nv_bfloat16*>(y);
-  if (chunks)
-    conv_fwd_kernel<true><<<grid, kConvThreads, 0, st>>>(xp, x_stride, wp, bp, sp, has_init, cu,
-                                                         chunks, num_chunks, T, C, N, silu, yp);
-  else
-    conv_fwd_kernel<false><<<grid, kConvThreads, 0, st>>>(xp, x_stride, wp, bp, sp, has_init, cu,
-                                                          nullptr, nullptr, T, C, N, silu, yp);
+  static const int num_sms = [] {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(conv_fwd_stream_kernel<true>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCvSmem);
+    cudaFuncSetAttribute(conv_fwd_stream_kernel<false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCvSmem);
+    return n > 0 ? n : 1;
+  }();
+  const int NB = (C + kCvChan - 1) / kCvChan;
+  const int R = std::max(1, std::min(num_sms / NB, (int)units));
+  auto kern = silu ? conv_fwd_stream_kernel<true> : conv_fwd_stream_kernel<false>;
+  kern<<<NB * R, kCvThreads, kCvSmem, st>>>(
+      static_cast<const __nv_bfloat16*>(x), x_stride, static_cast<const __nv_bfloat16*>(w),
+      static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(conv_state), has_init,
+      cu, chunks, num_chunks, units, T, C, N, static_cast<__nv_bfloat16*>(y));
   return check_launch();
 }
 

@@ -38,13 +38,70 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return u;
 }
 
+// ---------------------------------------------------------------------------
+// Pairs of float32 on the packed f32x2 FMA-pipe instructions of sm_100+ (one
+// instruction for both halves; each half rounds exactly as the scalar op).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t f2_bits(float2 v) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_from_bits(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return f2_from_bits(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return f2_from_bits(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return f2_from_bits(d);
+}
+// Two BF16 values of a packed word as a float pair (exact).
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ uint32_t f2_bf16x2(float2 v) { return pack_bf16x2(v.x, v.y); }
+
 // Read-only 16-byte global load (non-coherent path; inputs are never written
 // by the kernel that reads them).
 __device__ __forceinline__ uint4 ldg16(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+// SiLU(x) = x / (1 + e^-x) = x * 1 / (1 + 2^(-x log2 e)), on the hardware
+// base-2 exponential and reciprocal (ex2.approx.ftz, rcp.approx.ftz: a few
+// float32 ulps, far below the BF16 rounding of the result). Two special-
+// function operations and three FMA-pipe ones, where a libm-accurate exp and an
+// IEEE division cost several times more and made the conv prefill ALU-bound.
+// Large negative x gives 2^(+big) = inf, 1/inf = 0 and a (signed) zero result.
+__device__ __forceinline__ float silu_f(float x) {
+  float t, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+  return x * r;
+}
+
+// silu_f on a pair, the multiplies and the add as f32x2 instructions (the same
+// roundings as silu_f on each half).
+__device__ __forceinline__ float2 silu2(float2 x) {
+  const float2 t = mul2(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(t.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(t.y));
+  const float2 d = add2(e, make_float2(1.0f, 1.0f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(d.y));
+  return mul2(x, r);
+}
 
 // ---------------------------------------------------------------------------
 // Host-side helpers

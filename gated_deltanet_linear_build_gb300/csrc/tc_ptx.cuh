@@ -116,6 +116,21 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* mbar, uint32_t parit
   return ok;
 }
 
+// Bounded wait that backs off with __nanosleep between polls, so that a
+// waiting warp takes almost no issue slots from the working warps of its SM
+// sub-partition (a plain poll loop issues several instructions per poll).
+// Gives up after `max_polls` polls (each at least one poll instruction long;
+// about 2 s at the sleep lengths used here) and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* mbar, uint32_t parity,
+                                                unsigned sleep_ns = 32,
+                                                unsigned max_polls = 1u << 26) {
+  for (unsigned n = 0; n < max_polls; ++n) {
+    if (mbar_try_wait(mbar, parity)) return true;
+    __nanosleep(sleep_ns);
+  }
+  return false;
+}
+
 // Bounded wait for the phase with the given parity: gives up after about
 // `max_cycles` SM clock cycles and returns false (the caller records
 // GDN_ERR_TIMEOUT and unwinds).
