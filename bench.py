@@ -277,20 +277,58 @@ class Workload:
         self.prefill_tokens = sum(self.lengths)
         self.decode_tokens = DECODE_STEPS * N_SEQS
         self.tokens = self.prefill_tokens + self.decode_tokens
+        # Each step's conv descriptors, built once here for the per-kind timing
+        # (the sweep itself rebuilds them into the stack's buffer every step).
+        from gated_deltanet_linear_build_gb300 import gdn
+        self.step_chunks = []
+        for (cu, has, first, n, T) in self.meta:
+            ch = torch.empty((T // 8 + n, 4), dtype=torch.int32, device=device)
+            cnt = torch.empty((1,), dtype=torch.int32, device=device)
+            gdn.build_conv_chunks(cu, ch, cnt, chunk_tokens=8)
+            self.step_chunks.append((ch, cnt))
 
     def chunk_lengths(self):
         return [min(CHUNK, s.length - CHUNK * j) for st in self.steps for s in st.segments
                 for j in range(-(-s.length // CHUNK))]
 
-    def sweep(self, timer=None):
+    def sweep(self):
         """Enqueue one full sweep (all prefill steps, then all decode steps)."""
         for i, (cu, has, first, n, T) in enumerate(self.meta):
             ys = [y[:T] for y in self.py]
             os_ = [o[:T] for o in self.po]
-            self.stack.prefill_step(cu, has, first, n, self.px[i], self.pg[i], ys, os_,
-                                    timer=timer)
+            self.stack.prefill_step(cu, has, first, n, self.px[i], self.pg[i], ys, os_)
         for j in range(DECODE_STEPS):
-            self.stack.decode_step(self.dx[j], self.dg[j], self.dy, self.do, timer=timer)
+            self.stack.decode_step(self.dx[j], self.dg[j], self.dy, self.do)
+
+    def kind_launches(self, kind):
+        """Library calls of one kind in a sweep."""
+        return {"build_chunks": len(self.meta), "conv_prefill": LAYERS * len(self.meta),
+                "delta_prefill": LAYERS * len(self.meta), "conv_update": LAYERS * DECODE_STEPS,
+                "delta_decode": LAYERS * DECODE_STEPS}[kind]
+
+    def kind_sweep(self, kind):
+        """Every call of one kind that a sweep makes, on the same buffers and
+        shapes, back to back (for per-kind launch durations)."""
+        st = self.stack
+        for i, (cu, has, first, n, T) in enumerate(self.meta):
+            if kind == "build_chunks":
+                st.build_chunks(cu)
+            for l in range(LAYERS):
+                if kind == "conv_prefill":
+                    ch, cnt = self.step_chunks[i]
+                    st.conv_prefill_layer(l, cu, has, first, n, self.px[i][l], self.py[l][:T],
+                                          chunks=ch, num_chunks=cnt)
+                elif kind == "delta_prefill":
+                    a, b = self.pg[i][l]
+                    st.delta_prefill_layer(l, cu, has, first, n, self.py[l][:T], a, b,
+                                           self.po[l][:T])
+        for j in range(DECODE_STEPS):
+            for l in range(LAYERS):
+                if kind == "conv_update":
+                    st.conv_update_layer(l, self.dx[j][l], self.dy[l])
+                elif kind == "delta_decode":
+                    a, b = self.dg[j][l]
+                    st.delta_decode_layer(l, self.dy[l], a, b, self.do[l])
 
 
 class E2EWorkload:
@@ -350,32 +388,6 @@ class E2EWorkload:
                 self.hdo[l].copy_(wl.do[l], non_blocking=True)
                 d2h += N_SEQS * HV * D * 2
         self.h2d, self.d2h = h2d, d2h
-
-
-class EventTimer:
-    """Timing events around every library call, recorded as event nodes of
-    the captured graph (so each replay re-records them on the launch stream)."""
-
-    def __init__(self, torch):
-        self.torch = torch
-        self.ev = {k: ([], []) for k in KINDS}
-
-    def __call__(self, kind, edge):
-        e = self.torch.cuda.Event(enable_timing=True, external=True)
-        e.record(self.torch.cuda.current_stream())
-        self.ev[kind][0 if edge == "start" else 1].append(e)
-
-    def durations_ms(self, kind):
-        s, e = self.ev[kind]
-        return [a.elapsed_time(b) for a, b in zip(s, e)]
-
-
-def events_supported(torch) -> bool:
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        return True
-    except TypeError:
-        return False
 
 
 # ----------------------------------------------------------------------------
@@ -458,14 +470,12 @@ def run_reference(args):
 # The GPU arm
 # ----------------------------------------------------------------------------
 
-def kernel_report(wl, timer, hbm_peak, bf16_peak):
+def kernel_report(wl, kind_ms, hbm_peak, bf16_peak):
     """Per kind: launches, average duration, share of the sweep, and achieved
-    rate against its roofline (algorithmic work / average duration)."""
+    rate against its roofline (algorithmic work / average duration).
+    kind_ms[k] is the device time of all of a sweep's calls of kind k."""
     rep = {}
-    total = 0.0
-    durs = {k: timer.durations_ms(k) for k in KINDS}
-    for k in KINDS:
-        total += sum(durs[k])
+    total = sum(kind_ms.values())
     n_steps = len(wl.steps)
     chunk_fl = prefill_flops(wl.chunk_lengths()) / n_steps
     work = {
@@ -476,11 +486,9 @@ def kernel_report(wl, timer, hbm_peak, bf16_peak):
         "delta_prefill": ("tensor", chunk_fl),
     }
     for k in KINDS:
-        if not durs[k]:
-            continue
-        avg = statistics.mean(durs[k])
-        r = {"launches": len(durs[k]), "avg_us": avg * 1e3,
-             "share": sum(durs[k]) / total if total else None}
+        n = wl.kind_launches(k)
+        avg = kind_ms[k] / n
+        r = {"launches": n, "avg_us": avg * 1e3, "share": kind_ms[k] / total if total else None}
         if k in work:
             bound, amount = work[k]
             if bound == "hbm":
@@ -509,7 +517,6 @@ def run_gdn(args):
     hbm_peak, bf16_peak, _bf16_sus, peak_src = load_peaks()
     wl = Workload(rank, dev)
     stream = torch.cuda.Stream(device=dev)
-    timer = EventTimer(torch) if events_supported(torch) else None
 
     with torch.cuda.stream(stream):
         wl.sweep()                      # eager warm run (sets kernel attributes)
@@ -519,24 +526,38 @@ def run_gdn(args):
     with torch.cuda.graph(graph, stream=stream):
         wl.sweep()
     launches_per_sweep = wl.stack.launches - launches_before
-    tgraph = None                       # the same sweep with event nodes per call
-    if timer is not None:
-        tgraph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(tgraph, stream=stream):
-            wl.sweep(timer)
+    kind_graphs = {}                    # the same calls grouped by kind, one graph each
+    for k in KINDS:
+        with torch.cuda.stream(stream):
+            wl.kind_sweep(k)
+        torch.cuda.synchronize()
+        kind_graphs[k] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kind_graphs[k], stream=stream):
+            wl.kind_sweep(k)
 
-    for _ in range(args.warmup):
-        graph.replay()
+    # Replays go to the stream the events are recorded on.
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        for k in KINDS:
+            kind_graphs[k].replay()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    kev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for k in KINDS}
+    with ClockSampler(local) as clocks, torch.cuda.stream(stream):
         torch.cuda.synchronize()
         start.record(stream)
-        for i in range(args.steps):
-            # the last timed sweep is the instrumented one (per-kernel durations)
-            (tgraph if (tgraph is not None and i == args.steps - 1) else graph).replay()
+        for i in range(args.steps - 1):
+            graph.replay()
+        # The last timed step makes the same calls grouped by kind, with events
+        # around each group: per-kind launch durations without per-call events.
+        for k in KINDS:
+            kev[k][0].record(stream)
+            kind_graphs[k].replay()
+            kev[k][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
     if dist is not None:
@@ -545,8 +566,9 @@ def run_gdn(args):
     ms_max = reduce_over_ranks(ms, "max", dist, dev)
     tokens_all = reduce_over_ranks(float(wl.tokens), "sum", dist, dev)
     value = tokens_all / (ms_max / 1e3)
+    kind_ms = {k: kev[k][0].elapsed_time(kev[k][1]) for k in KINDS}
 
-    kernels = kernel_report(wl, timer, hbm_peak, bf16_peak) if timer else {}
+    kernels = kernel_report(wl, kind_ms, hbm_peak, bf16_peak)
     roofline = None
     if kernels:
         dom = max((k for k in kernels if "bound" in kernels[k]),
@@ -569,9 +591,10 @@ def run_gdn(args):
                    "prefill_steps": len(wl.steps), "step_tokens": STEP_TOKENS,
                    "conv_channels": C, "v_heads": HV, "qk_heads": HK, "head_dim": D,
                    "l2": "inputs larger than L2 (about 11 GB of distinct layer inputs per sweep)",
-                   "timing": "CUDA graph of one sweep (kernels only) replayed K-1 times, then "
-                             "once the same sweep with event nodes around every call (per-kernel "
-                             "times); CUDA events on the stream bracket all K",
+                   "timing": "CUDA graph of one sweep (kernels only) replayed K-1 times on the "
+                             "timing stream, then the same calls once more grouped by kernel kind "
+                             "(one graph per kind, CUDA events around each group: per-kind launch "
+                             "durations); CUDA events on the stream bracket all K",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roofline,
         "kernels": kernels,
@@ -587,16 +610,18 @@ def run_gdn(args):
         g2 = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g2, stream=stream):
             e2.sweep()
-        for _ in range(max(1, args.warmup)):
-            g2.replay()
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                g2.replay()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         s2, e2_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(args.steps):
-            g2.replay()
-        e2_.record(stream)
+        with torch.cuda.stream(stream):
+            s2.record(stream)
+            for _ in range(args.steps):
+                g2.replay()
+            e2_.record(stream)
         torch.cuda.synchronize()
         ms2 = reduce_over_ranks(s2.elapsed_time(e2_) / args.steps, "max", dist, dev)
         out["e2e"] = {"value": tokens_all / (ms2 / 1e3), "unit": "tokens/s",

@@ -183,7 +183,8 @@ __device__ __forceinline__ void store_state8(__nv_bfloat16* p, const float (&st)
 // descriptors [n r / R, n (r + 1) / R) of channel block cb. Every producer
 // warp reads the CTA's descriptors up front (one per lane) and walks the same
 // list of stages, kCvRows tokens each; stage i is posted by producer warp
-// i % kCvGroups into slot i % kCvStages of a shared-memory ring, with bulk
+// i % kCvGroups into that group's own ring of kCvSlotsPerGroup shared-memory
+// stages, with bulk
 // copies of the stage's rows, its 3-token halo (the 3 rows before it, or the
 // initial conv_state at the start of a sequence) and, on the first stage of a
 // sequence longer than the stage, the sequence's last 3 rows (the new
@@ -204,10 +205,21 @@ constexpr int kCvRows = 8;                               // tokens per stage
 constexpr int kCvSlot = kCvChan * 2;                     // one token's row segment (bytes)
 constexpr int kCvHalo = 0, kCvData = 3, kCvTail = 3 + kCvRows;   // slot indices
 constexpr int kCvStageBytes = (3 + kCvRows + 3) * kCvSlot;        // 28 KB
-constexpr int kCvStages = 7;
+// Each compute group has its own stages: a barrier is then only ever waited on
+// by one group, for its next phase. (With stages shared round-robin between
+// groups, a group that runs ahead can poll a barrier two phases before the one
+// it wants, and a parity wait cannot tell those phases apart.)
+constexpr int kCvSlotsPerGroup = 2;
+constexpr int kCvStages = kCvGroups * kCvSlotsPerGroup;
 constexpr int kCvMetaOff = kCvStages * kCvStageBytes;
 constexpr int kCvBarOff = kCvMetaOff + kCvStages * 32;
 constexpr int kCvSmem = kCvBarOff + 2 * kCvStages * 8;
+// Stage i: group i % kCvGroups, its use number u = i / kCvGroups, slot
+// g kCvSlotsPerGroup + u % kCvSlotsPerGroup, phase u / kCvSlotsPerGroup.
+__device__ __forceinline__ int cv_slot(int i) {
+  return (i % kCvGroups) * kCvSlotsPerGroup + (i / kCvGroups) % kCvSlotsPerGroup;
+}
+__device__ __forceinline__ int cv_round(int i) { return (i / kCvGroups) / kCvSlotsPerGroup; }
 // Stage flags.
 constexpr int kHaloX = 1;        // halo slots hold x rows tok-3 .. tok-1
 constexpr int kHaloState = 2;    // halo slots hold the initial conv_state [ch][3]
@@ -351,8 +363,8 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
         if (lane == 0) {
           for (int r0 = 0; r0 < len && ok; r0 += kCvRows, ++it) {
             if (it % kCvGroups != pw) continue;
-            const int st = it % kCvStages;
-            if (it >= kCvStages && !mbar_wait_sleep(empty + st, ((it / kCvStages) - 1) & 1, 128)) {
+            const int st = cv_slot(it), rd = cv_round(it);
+            if (rd > 0 && !mbar_wait_sleep(empty + st, (rd - 1) & 1, 128)) {
               ok = false;
               break;
             }
@@ -405,8 +417,8 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
     }
     if (lane == 0 && ok) {
       while (it % kCvGroups != pw) ++it;
-      const int st = it % kCvStages;
-      if (it < kCvStages || mbar_wait_sleep(empty + st, ((it / kCvStages) - 1) & 1, 128)) {
+      const int st = cv_slot(it), rd = cv_round(it);
+      if (rd == 0 || mbar_wait_sleep(empty + st, (rd - 1) & 1, 128)) {
         CvMeta m;
         m.rows = -1;
         post(m, 0, st);
@@ -446,9 +458,9 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
     }
   }
   for (int it = g;; it += kCvGroups) {
-    const int st = it % kCvStages;
+    const int st = cv_slot(it);
     // A wait that gives up (the producer stopped) ends the stream.
-    if (!mbar_wait_sleep(full + st, (it / kCvStages) & 1)) break;
+    if (!mbar_wait_sleep(full + st, cv_round(it) & 1)) break;
     const CvMeta m = meta[st];
     if (m.rows < 0) break;
     const unsigned char* stage = sm + st * kCvStageBytes;

@@ -137,34 +137,54 @@ class GdnLayerStack:
         gdn.build_conv_chunks(cu_d, self.chunks, self.num_chunks, chunk_tokens=8)
         self.launches += 1
 
+    def conv_prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, x, y,
+                           chunks=None, num_chunks=None):
+        """Layer l's conv prefill over a step's descriptors (the stack's own
+        buffer unless ``chunks``/``num_chunks`` are given)."""
+        sl = slice(first_slot, first_slot + n)
+        gdn.causal_conv1d_fwd(x, self.w[l], None, self.conv_state[l][sl], has_d, cu_d, y,
+                              chunks=self.chunks if chunks is None else chunks,
+                              num_chunks=self.num_chunks if num_chunks is None else num_chunks)
+        self.launches += 1
+
+    def delta_prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, y, a, b, out):
+        """Layer l's chunked delta rule on q/k/v read in place from the conv output y."""
+        sl = slice(first_slot, first_slot + n)
+        q, k, v = self.qkv(y)
+        gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, out,
+                                       self.workspace, qk_l2norm=True)
+        self.launches += PREFILL_LAUNCHES
+
+    def conv_update_layer(self, l: int, x, y):
+        gdn.causal_conv1d_update(x, self.w[l], None, self.conv_state[l], y)
+        self.launches += 1
+
+    def delta_decode_layer(self, l: int, y, a, b, out):
+        q, k, v = self.qkv(y)
+        gdn.delta_rule_decode(q, k, v, a, b, self.S[l], out, qk_l2norm=True)
+        self.launches += 1
+
     def prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, x, a, b, y, out,
                       tick=None):
         """Layer l of a prefill step: conv prefill over the step's descriptors,
         then the chunked delta rule on q/k/v read in place from the conv output."""
         tick = tick if tick is not None else (lambda kind, edge: None)
-        sl = slice(first_slot, first_slot + n)
         tick("conv_prefill", "start")
-        gdn.causal_conv1d_fwd(x, self.w[l], None, self.conv_state[l][sl], has_d, cu_d, y,
-                              chunks=self.chunks, num_chunks=self.num_chunks)
+        self.conv_prefill_layer(l, cu_d, has_d, first_slot, n, x, y)
         tick("conv_prefill", "end")
-        q, k, v = self.qkv(y)
         tick("delta_prefill", "start")
-        gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, out,
-                                       self.workspace, qk_l2norm=True)
+        self.delta_prefill_layer(l, cu_d, has_d, first_slot, n, y, a, b, out)
         tick("delta_prefill", "end")
-        self.launches += 1 + PREFILL_LAUNCHES
 
     def decode_layer(self, l: int, x, a, b, y, out, tick=None):
         """Layer l of a decode step: conv update, then the delta-rule decode."""
         tick = tick if tick is not None else (lambda kind, edge: None)
         tick("conv_update", "start")
-        gdn.causal_conv1d_update(x, self.w[l], None, self.conv_state[l], y)
+        self.conv_update_layer(l, x, y)
         tick("conv_update", "end")
-        q, k, v = self.qkv(y)
         tick("delta_decode", "start")
-        gdn.delta_rule_decode(q, k, v, a, b, self.S[l], out, qk_l2norm=True)
+        self.delta_decode_layer(l, y, a, b, out)
         tick("delta_decode", "end")
-        self.launches += 2
 
     # -- whole engine steps over precomputed layer inputs ------------------------
     def prefill_step(self, cu_d, has_d, first_slot: int, n: int, xs, gates, ys, outs,
