@@ -117,22 +117,69 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 // dk = dv = 128: persistent, warp-specialized streaming kernel. The state is
 // cut into units of 64 rows of one (sequence, v-head) -- 32 KB, contiguous --
 // and each CTA (one per SM) walks its units through a ring of shared-memory
-// stages. A producer warp issues, per unit, TMA bulk loads of the rows plus
-// the unit's k, q (256 B each) and v (128 B) into a stage, and later the bulk
-// stores of the updated rows and of the unit's 64 outputs; sixteen compute
-// warps wait on the stage's "full" barrier, update four rows each in place,
-// and arrive on its "empty" barrier. kDecStages units are in flight per SM.
+// stages. A producer warp issues, per unit, a TMA bulk load of the rows into a
+// stage, and later the bulk stores of the updated rows and of the unit's 64
+// outputs; sixteen compute warps wait on the stage's "full" barrier, update
+// four rows each in place, and arrive on its "empty" barrier.
+// The unit's k, q (128 values each) and v (64) sit beside its rows in the
+// stage. Unfused, the producer bulk-loads them from the conv output. Fused,
+// the conv update runs in the kernel: a second producer warp bulk-loads the
+// unit's conv inputs (x, state, taps, bias of its 320 channels) into a small
+// ring of their own, and ten conv warps (one channel per thread) convolve
+// them, write the BF16 outputs into the stage and the new conv state to
+// global memory, and arrive on the stage's "full" barrier: the compute warps
+// then run exactly as in the unfused kernel, one unit behind the conv warps.
 // ---------------------------------------------------------------------------
 constexpr int kDecRows = 64;                       // rows of S per unit
 constexpr int kDecUnitBytes = kDecRows * 128 * 4;  // 32 KB
-constexpr int kDecOffK = kDecUnitBytes, kDecOffQ = kDecOffK + 256, kDecOffV = kDecOffQ + 256;
-constexpr int kDecOffO = kDecOffV + 2 * kDecRows;  // BF16 outputs of the unit's rows
-constexpr int kDecStageBytes = kDecOffO + 2 * kDecRows;
+constexpr int kDecOffO = kDecUnitBytes;            // BF16 outputs of the unit's rows
+constexpr int kDecOffK = kDecOffO + 2 * kDecRows;  // k, q (256 B each) and v (128 B)
+constexpr int kDecOffQ = kDecOffK + 256, kDecOffV = kDecOffQ + 256;
+constexpr int kDecStageBytes = kDecOffV + 2 * kDecRows;
 constexpr int kDecStages = 6;
 constexpr int kDecWarps = 16;                      // compute warps, 4 rows each
-constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + producer warp
-constexpr int kDecSmem = kDecStages * kDecStageBytes + 2 * kDecStages * 8 + 64;
 constexpr int kDecUnitsPerHead = 128 / kDecRows;
+// Fused mode: conv-input slots, per q / k / v block of the unit's channels
+// (128 / 128 / 64): x and the state [ch][3]. Offsets in a slot. (The taps and
+// bias, the same for every sequence, are read through the cache by the conv
+// warps themselves.)
+constexpr int kFxQ = 0, kFxK = kFxQ + 256, kFxV = kFxK + 256;
+constexpr int kFsQ = kFxV + 128, kFsK = kFsQ + 768, kFsV = kFsK + 768;
+constexpr int kFSlot = kFsV + 384;                 // 2560 bytes
+constexpr int kFSlots = 6;
+constexpr int kFConv = 320;                        // conv channels of a unit (q, k, v)
+constexpr int kFConvWarps = kFConv / 32;           // 10
+constexpr int kFYSlot = 640;                       // BF16 k | q | v of a unit (fused)
+constexpr int kFYSlots = 4;
+template <bool kFused>
+struct DecStage {
+  static constexpr int kConvOff = kDecStages * kDecStageBytes;            // fused: conv ring
+  static constexpr int kYOff = kConvOff + (kFused ? kFSlots * kFSlot : 0);  // fused: y ring
+  static constexpr int kBarOff = kYOff + (kFused ? kFYSlots * kFYSlot : 0);
+  static constexpr int kSmem = kBarOff + 2 * (kDecStages + kFSlots + kFYSlots) * 8 + 64;
+  // compute warps, state producer, [conv-input producer, conv warps]
+  static constexpr int kProdWarp = kDecWarps;
+  static constexpr int kConvWarp0 = kDecWarps + 2;
+  static constexpr int kWarps = kDecWarps + 1 + (kFused ? 1 + kFConvWarps : 0);
+  static constexpr int kThreads = kWarps * 32;
+};
+
+// Arguments of the streaming decode kernels (both modes).
+struct DecodeArgs {
+  // unfused: q, k, v read from the conv output
+  const __nv_bfloat16 *q, *k, *v;
+  int64_t qk_stride, v_stride;
+  // fused: the conv update runs in the kernel (x, taps, bias, states)
+  const __nv_bfloat16 *x, *w, *bias, *st_in;
+  __nv_bfloat16* st_out;
+  int64_t x_stride;
+  int C, silu;
+  // both
+  const float *a, *b;
+  float* S;
+  __nv_bfloat16* o;
+  int Hk, Hv, qk_l2norm, units;
+};
 
 // Sum over the 32 lanes of eight per-lane values at once (transpose-reduce):
 // after five exchange rounds lane l holds the full sum of value (l >> 2) & 7
@@ -162,51 +209,154 @@ __device__ __forceinline__ float reduce8_transpose(const float (&x)[8], int lane
   return y1;   // value index m = 4 (lane & 16 ? 1 : 0) + 2 (lane & 8 ? 1 : 0) + (lane & 4 ? 1 : 0)
 }
 
-__global__ void __launch_bounds__(kDecThreads, 1)
-delta_decode_stream_kernel(const __nv_bfloat16* __restrict__ q,
-                           const __nv_bfloat16* __restrict__ k, int64_t qk_stride,
-                           const __nv_bfloat16* __restrict__ v, int64_t v_stride,
-                           const float* __restrict__ a, const float* __restrict__ b,
-                           float* __restrict__ S, __nv_bfloat16* __restrict__ o, int Hk, int Hv,
-                           int qk_l2norm, int units) {
+template <bool kFused>
+__global__ void __launch_bounds__(DecStage<kFused>::kThreads, 1)
+delta_decode_stream_kernel(const DecodeArgs p) {
   using namespace tc;
+  using Cfg = DecStage<kFused>;
   extern __shared__ __align__(128) unsigned char sm[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kDecStages * kDecStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Cfg::kBarOff);
   uint64_t* empty = full + kDecStages;
+  uint64_t* cfull = empty + kDecStages;    // fused: conv-input ring
+  uint64_t* cempty = cfull + kFSlots;
+  uint64_t* yfull = cempty + kFSlots;      // fused: conv-output ring
+  uint64_t* yempty = yfull + kFYSlots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
-  const int my_units = (units - (int)blockIdx.x + G - 1) / G;   // units blockIdx.x + i G
+  const int Hv = p.Hv, ratio = p.Hv / p.Hk;
+  const int my_units = (p.units - (int)blockIdx.x + G - 1) / G;   // units blockIdx.x + i G
   if (tid == 0) {
     for (int st = 0; st < kDecStages; ++st) {
       mbar_init(full + st, 1);
       mbar_init(empty + st, kDecWarps);
     }
+    if constexpr (kFused) {
+      for (int cs = 0; cs < kFSlots; ++cs) {
+        mbar_init(cfull + cs, 1);
+        mbar_init(cempty + cs, kFConvWarps);
+      }
+      for (int ys = 0; ys < kFYSlots; ++ys) {
+        mbar_init(yfull + ys, kFConvWarps);
+        mbar_init(yempty + ys, kDecWarps);
+      }
+    }
   }
   __syncthreads();
+  auto unit_coords = [&](int unit, int& n, int& h, int& g, int& part) {
+    const int nh = unit / kDecUnitsPerHead;
+    part = unit - nh * kDecUnitsPerHead;
+    n = nh / Hv;
+    h = nh - n * Hv;
+    g = h / ratio;
+  };
 
-  if (warp == kDecWarps) {
-    // Producer warp (lane 0 issues).
+  if constexpr (kFused) {
+    if (warp == Cfg::kProdWarp + 1) {
+      // Conv-input producer (lane 0): x, state, taps and bias of the unit's
+      // q, k and v channels into the conv ring.
+      if (lane == 0) {
+        for (int i = 0; i < my_units; ++i) {
+          const int cs = i % kFSlots;
+          if (i >= kFSlots && !mbar_wait(cempty + cs, ((i / kFSlots) - 1) & 1)) break;
+          int n, h, g, part;
+          unit_coords(blockIdx.x + i * G, n, h, g, part);
+          unsigned char* dst = sm + Cfg::kConvOff + cs * kFSlot;
+          const int cq = g * 128, ck = p.Hk * 128 + g * 128;
+          const int cv = 2 * p.Hk * 128 + h * 128 + part * kDecRows;
+          const __nv_bfloat16* xr = p.x + n * p.x_stride;
+          const __nv_bfloat16* sr = p.st_in + (size_t)n * p.C * 3;
+          uint64_t* bar = cfull + cs;
+          mbar_arrive_expect_tx(bar, 640 + 1920);
+          bulk_g2s(dst + kFxQ, xr + cq, 256, bar);
+          bulk_g2s(dst + kFxK, xr + ck, 256, bar);
+          bulk_g2s(dst + kFxV, xr + cv, 128, bar);
+          bulk_g2s(dst + kFsQ, sr + (size_t)cq * 3, 768, bar);
+          bulk_g2s(dst + kFsK, sr + (size_t)ck * 3, 768, bar);
+          bulk_g2s(dst + kFsV, sr + (size_t)cv * 3, 384, bar);
+        }
+      }
+      return;
+    }
+    if (warp >= Cfg::kConvWarp0 && warp < Cfg::kConvWarp0 + kFConvWarps) {
+      // Conv warps: channel t of the unit (q 0-127, k 128-255, v 256-319).
+      const int t = tid - Cfg::kConvWarp0 * 32;
+      const int blk = t < 128 ? 0 : (t < 256 ? 1 : 2);
+      const int c = t - 128 * blk;
+      const int offx = blk == 0 ? kFxQ : (blk == 1 ? kFxK : kFxV);
+      const int offs = blk == 0 ? kFsQ : (blk == 1 ? kFsK : kFsV);
+      // y slot: k 0-255, q 256-511, v 512-639 (BF16)
+      const int offy = blk == 0 ? 256 : (blk == 1 ? 0 : 512);
+      for (int i = 0; i < my_units; ++i) {
+        const int cs = i % kFSlots, ys = i % kFYSlots;
+        int n, h, g, part;
+        unit_coords(blockIdx.x + i * G, n, h, g, part);
+        const int cg = blk == 0 ? g * 128 + c
+                                : (blk == 1 ? p.Hk * 128 + g * 128 + c
+                                            : 2 * p.Hk * 128 + h * 128 + part * kDecRows + c);
+        // taps 0-3 and bias of global channel cg (issued before the wait)
+        const uint2 wu = __ldg(reinterpret_cast<const uint2*>(p.w) + cg);
+        const float bias = p.bias ? __bfloat162float(p.bias[cg]) : 0.f;
+        if (!mbar_wait_sleep(cfull + cs, (i / kFSlots) & 1, 64)) break;
+        const unsigned char* cslot = sm + Cfg::kConvOff + cs * kFSlot;
+        const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(cslot + offx);
+        const __nv_bfloat16* ss = reinterpret_cast<const __nv_bfloat16*>(cslot + offs);
+        const __nv_bfloat16 s1 = ss[3 * c + 1], s2 = ss[3 * c + 2], xbf = xs[c];
+        float acc = bias;
+        acc = fmaf(bf16lo(wu.x), __bfloat162float(ss[3 * c]), acc);
+        acc = fmaf(bf16hi(wu.x), __bfloat162float(s1), acc);
+        acc = fmaf(bf16lo(wu.y), __bfloat162float(s2), acc);
+        acc = fmaf(bf16hi(wu.y), __bfloat162float(xbf), acc);
+        const __nv_bfloat16 y = __float2bfloat16_rn(p.silu ? silu_f(acc) : acc);
+        __syncwarp();
+        if (lane == 0)   // this warp's conv inputs are read
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(cempty + cs)) : "memory");
+        // New state (s1, s2, x): v channels by every unit, q / k channels by
+        // one unit per (sequence, q/k head).
+        if (blk == 2 || (part == 0 && h % ratio == 0)) {
+          __nv_bfloat16* d = p.st_out + ((size_t)n * p.C + cg) * 3;
+          d[0] = s1;
+          d[1] = s2;
+          d[2] = xbf;
+        }
+        // The y slot is free once the compute warps have read its previous unit.
+        if (i >= kFYSlots && !mbar_wait_sleep(yempty + ys, ((i / kFYSlots) - 1) & 1, 64)) break;
+        reinterpret_cast<__nv_bfloat16*>(sm + Cfg::kYOff + ys * kFYSlot + offy)[c] = y;
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(yfull + ys)) : "memory");
+      }
+      return;
+    }
+  }
+
+  if (warp == Cfg::kProdWarp) {
+    // State producer (lane 0 issues).
     if (lane == 0) {
       auto issue_load = [&](int i) {
         const int st = i % kDecStages;
         const int unit = blockIdx.x + i * G;
-        const int nh = unit / kDecUnitsPerHead, part = unit - nh * kDecUnitsPerHead;
-        const int n = nh / Hv, h = nh - n * Hv, g = h / (Hv / Hk);
         unsigned char* dst = sm + st * kDecStageBytes;
-        mbar_arrive_expect_tx(full + st, kDecUnitBytes + 256 + 256 + 2 * kDecRows);
-        bulk_g2s(dst, S + (size_t)unit * kDecRows * 128, kDecUnitBytes, full + st);
-        bulk_g2s(dst + kDecOffK, k + n * qk_stride + (int64_t)g * 128, 256, full + st);
-        bulk_g2s(dst + kDecOffQ, q + n * qk_stride + (int64_t)g * 128, 256, full + st);
-        bulk_g2s(dst + kDecOffV, v + n * v_stride + (int64_t)h * 128 + part * kDecRows,
-                 2 * kDecRows, full + st);
+        if constexpr (kFused) {
+          mbar_arrive_expect_tx(full + st, kDecUnitBytes);   // k, q, v: the conv warps
+          bulk_g2s(dst, p.S + (size_t)unit * kDecRows * 128, kDecUnitBytes, full + st);
+        } else {
+          int n, h, g, part;
+          unit_coords(unit, n, h, g, part);
+          mbar_arrive_expect_tx(full + st, kDecUnitBytes + 256 + 256 + 2 * kDecRows);
+          bulk_g2s(dst, p.S + (size_t)unit * kDecRows * 128, kDecUnitBytes, full + st);
+          bulk_g2s(dst + kDecOffK, p.k + n * p.qk_stride + (int64_t)g * 128, 256, full + st);
+          bulk_g2s(dst + kDecOffQ, p.q + n * p.qk_stride + (int64_t)g * 128, 256, full + st);
+          bulk_g2s(dst + kDecOffV, p.v + n * p.v_stride + (int64_t)h * 128 + part * kDecRows,
+                   2 * kDecRows, full + st);
+        }
       };
       for (int i = 0; i < my_units && i < kDecStages; ++i) issue_load(i);
       for (int i = 0; i < my_units; ++i) {
         const int st = i % kDecStages;
         mbar_wait(empty + st, (i / kDecStages) & 1);
         const int unit = blockIdx.x + i * G;
-        bulk_s2g(S + (size_t)unit * kDecRows * 128, sm + st * kDecStageBytes, kDecUnitBytes);
-        bulk_s2g(o + (size_t)unit * kDecRows, sm + st * kDecStageBytes + kDecOffO, 2 * kDecRows);
+        bulk_s2g(p.S + (size_t)unit * kDecRows * 128, sm + st * kDecStageBytes, kDecUnitBytes);
+        bulk_s2g(p.o + (size_t)unit * kDecRows, sm + st * kDecStageBytes + kDecOffO, 2 * kDecRows);
         bulk_commit();
         // Refill the stage stored one unit ago (its store has had a unit's
         // time to read shared memory), keeping kDecStages - 1 loads in flight.
@@ -220,25 +370,42 @@ delta_decode_stream_kernel(const __nv_bfloat16* __restrict__ q,
     return;
   }
 
-  // Compute warps: rows 4 warp .. 4 warp + 3 of every unit.
+  // Compute warps: rows 4 warp .. 4 warp + 3 of every unit; lane l holds
+  // columns 4 l .. 4 l + 3.
   float a_nxt = 0.f, b_nxt = 0.f;
   if (my_units > 0) {
-    a_nxt = __ldg(a + blockIdx.x / kDecUnitsPerHead);
-    b_nxt = __ldg(b + blockIdx.x / kDecUnitsPerHead);
+    a_nxt = __ldg(p.a + blockIdx.x / kDecUnitsPerHead);
+    b_nxt = __ldg(p.b + blockIdx.x / kDecUnitsPerHead);
   }
   for (int i = 0; i < my_units; ++i) {
     const int st = i % kDecStages;
     const int unit = blockIdx.x + i * G;
     const float av = a_nxt, bv = b_nxt;
     if (i + 1 < my_units) {
-      a_nxt = __ldg(a + (unit + G) / kDecUnitsPerHead);
-      b_nxt = __ldg(b + (unit + G) / kDecUnitsPerHead);
+      a_nxt = __ldg(p.a + (unit + G) / kDecUnitsPerHead);
+      b_nxt = __ldg(p.b + (unit + G) / kDecUnitsPerHead);
     }
-    mbar_wait(full + st, (i / kDecStages) & 1);
+    // Waiting warps back off, so they take no issue slots from the producer
+    // warps on their sub-partition.
+    mbar_wait_sleep(full + st, (i / kDecStages) & 1, 32);
     unsigned char* stage = sm + st * kDecStageBytes;
-    const uint2 ku = reinterpret_cast<const uint2*>(stage + kDecOffK)[lane];
-    const uint2 qu = reinterpret_cast<const uint2*>(stage + kDecOffQ)[lane];
-    const uint2 vu = reinterpret_cast<const uint2*>(stage + kDecOffV)[warp];
+    uint2 ku, qu, vu;
+    if constexpr (kFused) {
+      // k, q, v from the conv warps' ring (BF16, as the unfused stage holds them)
+      const int ys = i % kFYSlots;
+      mbar_wait_sleep(yfull + ys, (i / kFYSlots) & 1, 32);
+      const unsigned char* yslot = sm + Cfg::kYOff + ys * kFYSlot;
+      ku = reinterpret_cast<const uint2*>(yslot)[lane];
+      qu = reinterpret_cast<const uint2*>(yslot + 256)[lane];
+      vu = reinterpret_cast<const uint2*>(yslot + 512)[warp];
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(yempty + ys)) : "memory");
+    } else {
+      ku = reinterpret_cast<const uint2*>(stage + kDecOffK)[lane];
+      qu = reinterpret_cast<const uint2*>(stage + kDecOffQ)[lane];
+      vu = reinterpret_cast<const uint2*>(stage + kDecOffV)[warp];
+    }
     float4 k4 = make_float4(bf16lo(ku.x), bf16hi(ku.x), bf16lo(ku.y), bf16hi(ku.y));
     float4 q4 = make_float4(bf16lo(qu.x), bf16hi(qu.x), bf16lo(qu.y), bf16hi(qu.y));
     const float vv[4] = {bf16lo(vu.x), bf16hi(vu.x), bf16lo(vu.y), bf16hi(vu.y)};
@@ -269,7 +436,7 @@ delta_decode_stream_kernel(const __nv_bfloat16* __restrict__ q,
       sq[j] = __shfl_sync(0xffffffffu, red, 16 + 4 * j);
     }
     float rk = 1.f, rq = 1.f;
-    if (qk_l2norm) {
+    if (p.qk_l2norm) {
       rk = 1.0f / sqrtf(kk + 1e-6f);
       rq = 1.0f / sqrtf(qq + 1e-6f);
     }
@@ -328,7 +495,55 @@ gdn_status_t launch_decode_dv(int dv, const void* q, const void* k, int64_t qk_s
   return GDN_ERR_UNSUPPORTED;
 }
 
+int decode_sm_count() {
+  static const int n = [] {
+    int dev = 0, c = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    cudaFuncSetAttribute(delta_decode_stream_kernel<false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, DecStage<false>::kSmem);
+    cudaFuncSetAttribute(delta_decode_stream_kernel<true>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, DecStage<true>::kSmem);
+    return c > 0 ? c : 1;
+  }();
+  return n;
+}
+
+template <bool kFused>
+gdn_status_t launch_decode_stream(const DecodeArgs& p, cudaStream_t st) {
+  const int sms = decode_sm_count();
+  const int grid = p.units < sms ? p.units : sms;
+  delta_decode_stream_kernel<kFused>
+      <<<grid, DecStage<kFused>::kThreads, DecStage<kFused>::kSmem, st>>>(p);
+  return check_launch();
+}
+
 }  // namespace
+
+gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
+                                 const void* bias, const void* st_in, void* st_out,
+                                 const float* a, const float* b, float* S, void* o, int32_t N,
+                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t qk_l2norm,
+                                 cudaStream_t st) {
+  DecodeArgs p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.w = static_cast<const __nv_bfloat16*>(w);
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.st_in = static_cast<const __nv_bfloat16*>(st_in);
+  p.st_out = static_cast<__nv_bfloat16*>(st_out);
+  p.x_stride = x_stride;
+  p.C = 2 * Hk * 128 + Hv * 128;
+  p.silu = silu;
+  p.a = a;
+  p.b = b;
+  p.S = S;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.Hk = Hk;
+  p.Hv = Hv;
+  p.qk_l2norm = qk_l2norm;
+  p.units = N * Hv * kDecUnitsPerHead;
+  return launch_decode_stream<true>(p, st);
+}
 
 gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride,
                                  const void* v, int64_t v_stride, const float* a,
@@ -336,21 +551,21 @@ gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
                                  cudaStream_t st) {
   if (dk == 128 && dv == 128) {
-    static const int num_sms = [] {
-      int dev = 0, n = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      cudaFuncSetAttribute(delta_decode_stream_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
-      return n > 0 ? n : 1;
-    }();
-    const int units = N * Hv * kDecUnitsPerHead;
-    const int grid = units < num_sms ? units : num_sms;
-    delta_decode_stream_kernel<<<grid, kDecThreads, kDecSmem, st>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride,
-        static_cast<const __nv_bfloat16*>(v), v_stride, a, b, S, static_cast<__nv_bfloat16*>(o),
-        Hk, Hv, qk_l2norm, units);
-    return check_launch();
+    DecodeArgs p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.qk_stride = qk_stride;
+    p.v_stride = v_stride;
+    p.a = a;
+    p.b = b;
+    p.S = S;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.Hk = Hk;
+    p.Hv = Hv;
+    p.qk_l2norm = qk_l2norm;
+    p.units = N * Hv * kDecUnitsPerHead;
+    return launch_decode_stream<false>(p, st);
   }
   switch (dk) {
     case 16: return launch_decode_dv<16>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st);

@@ -135,6 +135,35 @@ gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stri
                              qk_l2norm, static_cast<cudaStream_t>(stream));
 }
 
+gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* w,
+                                   const void* bias, const void* conv_state_in,
+                                   void* conv_state_out, const float* a, const float* b,
+                                   float* S, void* o, int32_t N, int32_t Hk, int32_t Hv,
+                                   int32_t dk, int32_t dv, int32_t K, int32_t silu,
+                                   int32_t qk_l2norm, void* stream) {
+  if (N < 0) return GDN_ERR_INVALID_ARG;
+  if (N == 0) return GDN_OK;
+  if (!x || !w || !conv_state_in || !conv_state_out || !a || !b || !S || !o)
+    return GDN_ERR_INVALID_ARG;
+  if (Hk <= 0 || Hv <= 0 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
+  if ((silu != 0 && silu != 1) || (qk_l2norm != 0 && qk_l2norm != 1)) return GDN_ERR_INVALID_ARG;
+  if (K != kConvTaps) return GDN_ERR_UNSUPPORTED;
+  if (dk != 128 || dv != 128) return GDN_ERR_UNSUPPORTED;
+  const int64_t C = 2 * (int64_t)Hk * dk + (int64_t)Hv * dv;
+  if (C > 0x7fffffff || (int64_t)N * Hv * 2 > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
+  if (x_stride < C) return GDN_ERR_INVALID_ARG;
+  if (x_stride % 8 != 0) return GDN_ERR_ALIGNMENT;
+  if (!aligned16(x) || !aligned16(w) || (bias && !aligned16(bias)) || !aligned16(conv_state_in) ||
+      !aligned16(conv_state_out) || !aligned16(S) || !aligned16(o))
+    return GDN_ERR_ALIGNMENT;
+  const uintptr_t si = reinterpret_cast<uintptr_t>(conv_state_in);
+  const uintptr_t so = reinterpret_cast<uintptr_t>(conv_state_out);
+  const uintptr_t sb = (uintptr_t)N * (uintptr_t)C * 3u * 2u;
+  if (si < so + sb && so < si + sb) return GDN_ERR_INVALID_ARG;   // the states overlap
+  return launch_decode_fused(x, x_stride, w, bias, conv_state_in, conv_state_out, a, b, S, o, N,
+                             Hk, Hv, silu, qk_l2norm, static_cast<cudaStream_t>(stream));
+}
+
 size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv, int32_t dk,
                                              int32_t dv, int32_t chunk) {
   return prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);

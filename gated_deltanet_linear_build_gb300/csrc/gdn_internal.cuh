@@ -142,6 +142,13 @@ gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
                                  cudaStream_t st);
 
+// Conv update and delta-rule decode in one launch (dk = dv = 128).
+gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
+                                 const void* bias, const void* st_in, void* st_out,
+                                 const float* a, const float* b, float* S, void* o, int32_t N,
+                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t qk_l2norm,
+                                 cudaStream_t st);
+
 size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                                int32_t chunk);
 

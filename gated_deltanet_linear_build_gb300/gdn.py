@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = (
     "gdn_causal_conv1d_fwd",
     "gdn_causal_conv1d_update",
     "gdn_delta_rule_decode",
+    "gdn_decode_step_fused",
     "gdn_delta_rule_prefill_workspace_size",
     "gdn_delta_rule_prefill_chunked",
     "gdn_delta_rule_prefill_chunked_noalloc",
@@ -59,6 +60,8 @@ _SIGNATURES = {
                                                 _P, _P]),
     "gdn_delta_rule_decode": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P, _I32, _I32,
                                              _I32, _I32, _I32, _I32, _P]),
+    "gdn_decode_step_fused": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32,
+                                             _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "gdn_delta_rule_prefill_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I32, _I32, _I32,
                                                                 _I32]),
     "gdn_delta_rule_prefill_chunked": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _I32,
@@ -163,6 +166,20 @@ def delta_rule_decode(q, k, v, a, b, S, o, *, qk_l2norm: bool = False, stream=No
                                       _ptr(a), _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk, dv,
                                       int(qk_l2norm), _stream(stream))
     _check(rc, "gdn_delta_rule_decode")
+
+
+def decode_step_fused(x, w, bias, conv_state_in, conv_state_out, a, b, S, o, *, Hk: int,
+                      silu: bool = True, qk_l2norm: bool = False, stream=None):
+    """Conv update and delta-rule decode in one launch. x [N, C] conv inputs
+    (C = 2 Hk d + Hv d), conv_state_in / conv_state_out [N, C, 3] (distinct
+    buffers), a, b [N, Hv], S [N, Hv, d, d] (in place), o [N, Hv, d]."""
+    N = x.shape[0]
+    Hv, dv, dk = S.shape[1], S.shape[2], S.shape[3]
+    rc = _lib().gdn_decode_step_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(bias),
+                                      _ptr(conv_state_in), _ptr(conv_state_out), _ptr(a),
+                                      _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk, dv, w.shape[1],
+                                      int(silu), int(qk_l2norm), _stream(stream))
+    _check(rc, "gdn_decode_step_fused")
 
 
 def delta_rule_prefill_workspace_size(T: int, N: int, Hv: int, dk: int, dv: int,

@@ -188,6 +188,38 @@ GDN_API gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t
                                    int32_t qk_l2norm, void* stream);
 
 /*
+ * One decode step of a GDN layer in a single launch: the conv update of
+ * gdn_causal_conv1d_update followed by gdn_delta_rule_decode on its output,
+ * without the conv output ever leaving the GPU's on-chip memory. Source: "RTX
+ * 5070 Ti ...", Existing evidence (the fused decode path, the post-conv step
+ * folded into its neighbours); here the conv update is the part folded in.
+ *
+ * The result equals the two calls in sequence, bit for bit: the conv output is
+ * rounded to BF16 exactly as gdn_causal_conv1d_update stores it, and q | k | v
+ * are its channels [0, Hk dk) | [Hk dk, 2 Hk dk) | [2 Hk dk, C).
+ *
+ *   x              BF16 [N, C] conv inputs, row stride x_stride (>= C, % 8 == 0),
+ *                  C = 2 Hk dk + Hv dv.
+ *   w, bias        BF16 [C, 4] taps and [C] bias or NULL, as for the conv calls.
+ *   conv_state_in  BF16 [N, C, 3]: the state before the step (read only).
+ *   conv_state_out BF16 [N, C, 3]: the state after it (written). The two must
+ *                  not overlap: several blocks read a q/k channel's old state
+ *                  while one of them writes its new one, so the update cannot be
+ *                  in place (callers alternate two buffers). Overlap is
+ *                  GDN_ERR_INVALID_ARG.
+ *   a, b, S, o     as for gdn_delta_rule_decode (S updated in place).
+ *   dk, dv         128 only (else GDN_ERR_UNSUPPORTED; use the two calls).
+ *   K              4.   silu, qk_l2norm: 0 or 1.
+ * All pointers 16-byte aligned.
+ */
+GDN_API gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* w,
+                                   const void* bias, const void* conv_state_in,
+                                   void* conv_state_out, const float* a, const float* b,
+                                   float* S, void* o, int32_t N, int32_t Hk, int32_t Hv,
+                                   int32_t dk, int32_t dv, int32_t K, int32_t silu,
+                                   int32_t qk_l2norm, void* stream);
+
+/*
  * Bytes of device workspace that gdn_delta_rule_prefill_chunked needs for these
  * sizes (0 for invalid sizes). Pure host arithmetic.
  */

@@ -135,3 +135,35 @@ def test_prefill_validation(lib):
     assert prefill(lib, ws=A16 * 16 + 16) == ALIGN              # workspace 256-byte rule
     assert prefill(lib, T=0) == OK
     assert prefill(lib, N=0) == OK
+
+
+def test_decode_step_fused_validation(lib):
+    f = lib.gdn_decode_step_fused
+    C = 2 * 16 * 128 + 32 * 128
+    N = 4
+    sb = N * C * 3 * 2                      # bytes of one conv state buffer
+    s_in, s_out = A16, A16 + 0x1000000      # disjoint fake buffers
+    args = dict(x=A16, xs=C, w=A16, bias=None, si=s_in, so=s_out, a=A16, b=A16, S=A16, o=A16,
+                N=N, Hk=16, Hv=32, dk=128, dv=128, K=4, silu=1, l2=1)
+
+    def call(**kw):
+        d = dict(args, **kw)
+        return f(d["x"], d["xs"], d["w"], d["bias"], d["si"], d["so"], d["a"], d["b"], d["S"],
+                 d["o"], d["N"], d["Hk"], d["Hv"], d["dk"], d["dv"], d["K"], d["silu"], d["l2"],
+                 None)
+
+    assert call(N=0) == OK                           # nothing to do, no launch
+    assert call(N=-1) == INVALID
+    assert call(x=None) == INVALID
+    assert call(so=None) == INVALID
+    assert call(so=s_in + sb - 16) == INVALID          # output state overlaps the input state
+    assert call(si=s_out + 16) == INVALID
+    assert call(Hv=24, Hk=16) == INVALID               # Hv % Hk != 0
+    assert call(silu=2) == INVALID
+    assert call(xs=C - 8) == INVALID                   # row stride shorter than C
+    assert call(dk=64, dv=64) == UNSUPPORTED           # the fused path is d = 128 only
+    assert call(K=3) == UNSUPPORTED
+    assert call(xs=C + 4) == ALIGN
+    assert call(x=A8) == ALIGN
+    assert call(bias=A8) == ALIGN
+    assert call(so=s_out + 8) == ALIGN
