@@ -476,7 +476,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   uint64_t* tbA = mbar + 1;   // W hi/lo + gates
   uint64_t* tbU = mbar + 2;   // U
   uint64_t* tbB = mbar + 3;   // P
-  uint64_t* obar = mbar + 4;  // a chunk's output MMAs
+  uint64_t* obar = mbar + 4;  // a chunk's output MMAs (O1 and O2)
+  uint64_t* qbar = mbar + 7;  // a chunk's O1 MMAs: the Q tile is free again
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 40);
   int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 44);
   int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 48);
@@ -497,6 +498,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     mbar_init(tbU, 1);
     mbar_init(tbB, 1);
     mbar_init(obar, 1);
+    mbar_init(qbar, 1);
   }
   __syncthreads();
   {
@@ -538,6 +540,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   };
   // Outstanding record copies (thread 0's view), for the bounded drain on exit.
   int pend_a = -1, pend_u = -1, pend_b = -1;
+  int pend_q = -1, pend_o = -1;   // MMA commits not yet waited for by thread 0
   auto copy_a = [&](int ci) {
     const unsigned char* rec = rec_of(ci);
     mbar_arrive_expect_tx(tbA, 32768 + 768);
@@ -670,15 +673,23 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(wh, 64, kk), idw, 1);
       mma_commit(mbar);   // X is what Delta waits for; O1 completes with the output barrier
       for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
+      mma_commit(qbar);   // the Q tile may be refilled once O1 has read it
+      pend_q = ci;
+      // P is read by the previous chunk's O2 MMAs (the output barrier): this
+      // chunk's P replaces it only after they are done.
+      if (ci >= 1) {
+        if (!mbar_wait(obar, (ci - 1) & 1)) atomicExch(s_fail, 1);
+        pend_o = -1;
+        copy_b(ci);
+      }
     }
     // Warps 4-7 write the previous chunk's outputs while these MMAs run.
     if (done > 0 && warp >= 4) write_outputs(ci - 1);
     if (!mbar_wait(mbar, phase)) atomicExch(s_fail, 1);
     phase ^= 1;
     fence_after_sync();
-    // W, the gates and the Q tile are free: fetch the next chunk's.
+    // W and the gates are free: fetch the next chunk's.
     if (tid == 0 && ci + 1 < nchunks) copy_a(ci + 1);
-    load_rows(ci + 1, q, kS2_Q);
     if (!mbar_wait(tbU, par)) atomicExch(s_fail, 1);
     if (tid == 0) pend_u = -1;
     fence_before_sync();
@@ -708,7 +719,12 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(row, s0, 64)) = lo;
       }
     }
-    cp_async_wait_group<1>();   // this chunk's K rows (the next Q rows may still be landing)
+    cp_async_wait_group<0>();   // this chunk's K rows
+    // The Q tile is read by this chunk's O1 MMAs, which the first barrier does
+    // not cover (long done by now): then the next chunk's Q rows replace it.
+    if (!mbar_wait(qbar, par)) atomicExch(s_fail, 1);
+    if (tid == 0) pend_q = -1;
+    load_rows(ci + 1, q, kS2_Q);
     fence_smem_to_async();
     fence_before_sync();
     __syncthreads();
@@ -728,6 +744,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         mma_commit(mbar);   // the next chunk needs only S
         for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + o2col, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, kk > 0);
         mma_commit(obar);
+        pend_o = ci;
       }
     }
     __syncthreads();
@@ -736,8 +753,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     phase ^= 1;
     fence_after_sync();
     done = ci + 1;
-    // P and the K tile are free: fetch the next chunk's.
-    if (tid == 0 && ci + 1 < nchunks) copy_b(ci + 1);
+    // The K tile is free (P is refilled after this chunk's O2, in the next
+    // chunk): fetch the next chunk's K rows.
     load_rows(ci + 1, k, kS2_K);
     fence_before_sync();
     __syncthreads();
@@ -764,6 +781,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (pend_a >= 0) mbar_wait(tbA, pend_a & 1);
     if (pend_u >= 0) mbar_wait(tbU, pend_u & 1);
     if (pend_b >= 0) mbar_wait(tbB, pend_b & 1);
+    if (pend_q >= 0) mbar_wait(qbar, pend_q & 1);
+    if (pend_o >= 0) mbar_wait(obar, pend_o & 1);
   }
   fence_before_sync();
   __syncthreads();
