@@ -69,6 +69,8 @@ build_chunks_kernel(const int32_t* __restrict__ cu, int n, int chunk,
   __shared__ int s_bad;
   __shared__ unsigned long long s_count;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     s_bad = (cu[0] != 0);
     s_count = 0;
@@ -303,6 +305,8 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
     }
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   if (warp >= kCvComputeWarps) {
     // Producer warp pw. Lanes fetch and validate 32 descriptors at a time;
@@ -545,6 +549,8 @@ conv_update_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                    const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ bias,
                    __nv_bfloat16* __restrict__ state, int C, int silu,
                    __nv_bfloat16* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int n = blockIdx.y;
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
   if (c0 >= C) return;
@@ -581,9 +587,8 @@ conv_update_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
 gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
                                  gdn_conv_chunk_t* chunks, int32_t capacity,
                                  int32_t* num_chunks, int32_t* status, cudaStream_t st) {
-  build_chunks_kernel<<<1, kBuildThreads, 0, st>>>(cu, n, chunk_tokens, chunks, capacity,
-                                                   num_chunks, status);
-  return check_launch();
+  return check_launch(launch_pdl(build_chunks_kernel, dim3(1), dim3(kBuildThreads), 0, st, cu, n,
+                                chunk_tokens, chunks, capacity, num_chunks, status));
 }
 
 gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, const void* bias,
@@ -605,22 +610,22 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
   const int NB = (C + kCvChan - 1) / kCvChan;
   const int R = std::max(1, std::min(num_sms / NB, (int)units));
   auto kern = silu ? conv_fwd_stream_kernel<true> : conv_fwd_stream_kernel<false>;
-  kern<<<NB * R, kCvThreads, kCvSmem, st>>>(
-      static_cast<const __nv_bfloat16*>(x), x_stride, static_cast<const __nv_bfloat16*>(w),
-      static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(conv_state), has_init,
-      cu, chunks, num_chunks, units, T, C, N, static_cast<__nv_bfloat16*>(y));
-  return check_launch();
+  return check_launch(launch_pdl(
+      kern, dim3(NB * R), dim3(kCvThreads), kCvSmem, st, static_cast<const __nv_bfloat16*>(x),
+      x_stride, static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(bias),
+      static_cast<__nv_bfloat16*>(conv_state), has_init, cu, chunks, num_chunks, (int)units,
+      (int)T, (int)C, (int)N, static_cast<__nv_bfloat16*>(y)));
 }
 
 gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
                                 const void* bias, void* conv_state, int32_t N, int32_t C,
                                 int32_t silu, void* y, cudaStream_t st) {
   dim3 grid((C / 8 + kConvThreads - 1) / kConvThreads, N);
-  conv_update_kernel<<<grid, kConvThreads, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), x_stride, static_cast<const __nv_bfloat16*>(w),
-      static_cast<const __nv_bfloat16*>(bias), static_cast<__nv_bfloat16*>(conv_state), C, silu,
-      static_cast<__nv_bfloat16*>(y));
-  return check_launch();
+  return check_launch(launch_pdl(
+      conv_update_kernel, grid, dim3(kConvThreads), 0, st, static_cast<const __nv_bfloat16*>(x),
+      x_stride, static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(bias),
+      static_cast<__nv_bfloat16*>(conv_state), (int)C, (int)silu,
+      static_cast<__nv_bfloat16*>(y)));
 }
 
 }  // namespace gdn

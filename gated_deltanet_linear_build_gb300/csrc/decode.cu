@@ -59,6 +59,8 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   using Cfg = DecodeCfg<DK, DV>;
   constexpr int LPR = Cfg::kLanesPerRow;
   __shared__ float s_o[DV];
+  pdl_wait();
+  pdl_trigger();
 
   const int nh = blockIdx.x;  // n * Hv + h
   const int n = nh / Hv, h = nh - n * Hv;
@@ -242,6 +244,8 @@ delta_decode_stream_kernel(const DecodeArgs p) {
     }
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   auto unit_coords = [&](int unit, int& n, int& h, int& g, int& part) {
     const int nh = unit / kDecUnitsPerHead;
     part = unit - nh * kDecUnitsPerHead;
@@ -475,11 +479,11 @@ gdn_status_t launch_decode_t(const void* q, const void* k, int64_t qk_stride, co
                              int64_t v_stride, const float* a, const float* b, float* S,
                              void* o, int N, int Hk, int Hv, int qk_l2norm, cudaStream_t st) {
   using Cfg = DecodeCfg<DK, DV>;
-  delta_decode_kernel<DK, DV><<<N * Hv, Cfg::kThreads, 0, st>>>(
+  return check_launch(launch_pdl(
+      delta_decode_kernel<DK, DV>, dim3(N * Hv), dim3(Cfg::kThreads), 0, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride,
-      static_cast<const __nv_bfloat16*>(v), v_stride, a, b, S,
-      static_cast<__nv_bfloat16*>(o), Hk, Hv, qk_l2norm);
-  return check_launch();
+      static_cast<const __nv_bfloat16*>(v), v_stride, a, b, S, static_cast<__nv_bfloat16*>(o),
+      Hk, Hv, qk_l2norm));
 }
 
 template <int DK>
@@ -513,9 +517,8 @@ template <bool kFused>
 gdn_status_t launch_decode_stream(const DecodeArgs& p, cudaStream_t st) {
   const int sms = decode_sm_count();
   const int grid = p.units < sms ? p.units : sms;
-  delta_decode_stream_kernel<kFused>
-      <<<grid, DecStage<kFused>::kThreads, DecStage<kFused>::kSmem, st>>>(p);
-  return check_launch();
+  return check_launch(launch_pdl(delta_decode_stream_kernel<kFused>, dim3(grid),
+                                dim3(DecStage<kFused>::kThreads), DecStage<kFused>::kSmem, st, p));
 }
 
 }  // namespace

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "gdn.h"
 
 namespace gdn {
@@ -118,6 +120,47 @@ inline gdn_status_t check_launch() {
     return GDN_ERR_CUDA;
   }
   return GDN_OK;
+}
+
+// Status of a launch call that returns its error (cudaLaunchKernelEx).
+inline gdn_status_t check_launch(cudaError_t e) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // clear it
+    set_cuda_error(e);
+    return GDN_ERR_CUDA;
+  }
+  return check_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel is launched with programmatic
+// stream serialisation: it may start while the previous kernel on the stream
+// is still finishing, runs only its own set-up (shared-memory barriers, tensor
+// memory) before pdl_wait(), which returns once that kernel has completed and
+// its writes are visible, and then lets the next kernel start launching
+// (pdl_trigger()). Because a kernel triggers only after its own wait, every
+// kernel two or more launches back has completed when a kernel starts. Without
+// the launch attribute both instructions are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Launchers implemented in the kernel translation units. They assume their

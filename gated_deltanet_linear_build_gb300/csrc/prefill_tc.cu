@@ -174,6 +174,8 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
   float* s_tot = reinterpret_cast<float*>(sm + kS1_BAR + 16);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   if ((int)blockIdx.x >= hdr[0]) return;
   const int4 d = reinterpret_cast<const int4*>(desc)[blockIdx.x];
   const int tok0 = d.y, n = d.z;
@@ -486,6 +488,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = 32 * (warp & 3) + lane;   // S row (dv index) = TMEM lane
   const int hf = warp >> 2;                 // column / token half
+  pdl_wait();
+  pdl_trigger();
   const int start = cu[seq], end = cu[seq + 1];
   if (start < 0 || end <= start || end > T) return;
   const int nchunks = (end - start + kC - 1) / kC;
@@ -814,15 +818,17 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
   if (cudaMemsetAsync(hdr + 2, 0, sizeof(int32_t), st) != cudaSuccess) return check_launch();
   gdn_status_t rc = launch_build_chunks(cu, N, kC, desc, L.capacity, hdr, hdr + 1, st);
   if (rc != GDN_OK) return rc;
-  tc_chunk_kernel<<<dim3(L.capacity, Hv), kThreads, kS1_BYTES, st>>>(
-      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(q), qk_stride,
-      static_cast<const __nv_bfloat16*>(v), v_stride, a, b, hdr, desc, T, Hk, Hv, qk_l2norm,
-      records, hdr);
-  if ((rc = check_launch()) != GDN_OK) return rc;
-  tc_state_kernel<<<dim3(N, Hv), kThreads2, kS2_BYTES, st>>>(
+  if ((rc = check_launch(launch_pdl(
+           tc_chunk_kernel, dim3(L.capacity, Hv), dim3(kThreads), kS1_BYTES, st,
+           static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(q), qk_stride,
+           static_cast<const __nv_bfloat16*>(v), v_stride, a, b, (const int32_t*)hdr, desc, T, Hk,
+           Hv, qk_l2norm, records, hdr))) != GDN_OK)
+    return rc;
+  return check_launch(launch_pdl(
+      tc_state_kernel, dim3(N, Hv), dim3(kThreads2), kS2_BYTES, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride, cu,
-      T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, records, hdr);
-  return check_launch();
+      T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, (const unsigned char*)records,
+      hdr));
 }
 
 }  // namespace gdn
