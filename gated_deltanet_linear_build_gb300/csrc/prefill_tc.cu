@@ -44,8 +44,10 @@ constexpr int kThreads = 128;
 
 // Record of one (chunk, v-head) written by the chunk kernel and read, by bulk
 // copy, by the state kernel.
-constexpr int kOffWhi = 0;          // W hi   MN-major B tile: N = token r (64), K = j (128)
-constexpr int kOffWlo = 16384;      // W lo
+// W hi and W lo as one MN-major B tile of N = 128 (rows 0-63: W hi of token r,
+// rows 64-127: W lo of token r), K = j (128), so that S_hi [W hi; W lo]^T is a
+// single N = 128 product.
+constexpr int kOffW = 0;
 constexpr int kOffP = 32768;        // P      K-major  [64 r][64 s]
 constexpr int kOffU = 40960;        // U      [128 i][64 r] float32, 16-byte chunks XOR-swizzled
 constexpr int kOffGK = 73728;       // g[64] (log2 of the cumulative decay), rk[64], rq[64]
@@ -397,9 +399,9 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
       for (int rg = 0; rg < 4; ++rg) {
         uint4 hi, lo;
         split8(w + 8 * rg, hi, lo);
-        const uint32_t off = mn_off(32 * half + 8 * rg, tid, 64);
-        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffWhi + off) = hi;
-        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffWlo + off) = lo;
+        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(32 * half + 8 * rg, tid, 128)) = hi;
+        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(64 + 32 * half + 8 * rg, tid, 128)) =
+            lo;
       }
     }
     // Lane i holds U[r][i] for all r: row i (float32), its 16-byte chunk c at
@@ -426,7 +428,7 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
   fence_before_sync();
   __syncthreads();
   if (tid == 0 && !*s_fail) {
-    bulk_s2g(rec + kOffWhi, sm + kS1_A1 + kOffWhi, 32768);
+    bulk_s2g(rec + kOffW, sm + kS1_A1 + kOffW, 32768);
     bulk_s2g(rec + kOffU, sm + kS1_V, 32768);
     bulk_s2g(rec + kOffGK, sm + kS1_RS, 768);
     bulk_commit();
@@ -439,7 +441,8 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 // State kernel: 256 threads. Warp w reads TMEM lanes 32 (w % 4) .. + 31 (row
 // i = lane of that quarter) and handles column half w / 4 of every row-wise
 // step, so each step is split over two warps per row.
-// TMEM: S in columns [0, 128), X^T in [128, 192), O1^T and O2^T double-buffered
+// TMEM: S in columns [0, 128), X^T in [128, 256) (two partial sums), O1^T and
+// O2^T double-buffered
 // in [256, 384) and [384, 512): a chunk's outputs are written back while the
 // next chunk's first MMA round runs.
 // Per chunk, the record arrives in three bulk copies issued as soon as the
@@ -456,7 +459,7 @@ constexpr int kS2_DDL = 98304;      // (Delta^T D) lo         16384
 constexpr int kS2_Q = 114688;       // Q rows [64 r][128 j] K-major B   16384
 constexpr int kS2_K = 131072;       // K rows [64 s][128 j] (MN-major B) 16384
 constexpr int kS2_R = 147456;       // the chunk's record
-constexpr int kS2_WH = kS2_R + kOffWhi, kS2_WL = kS2_R + kOffWlo, kS2_P = kS2_R + kOffP;
+constexpr int kS2_W = kS2_R + kOffW, kS2_P = kS2_R + kOffP;
 constexpr int kS2_U = kS2_R + kOffU, kS2_GK = kS2_R + kOffGK;
 constexpr int kS2_QS = kS2_R + kRecBytes;         // e^{g_r} rq_r, two chunks [2][64]
 constexpr int kS2_DK = kS2_QS + 512;              // e^{g_last - g_s} rk_s [64]
@@ -548,8 +551,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   auto copy_a = [&](int ci) {
     const unsigned char* rec = rec_of(ci);
     mbar_arrive_expect_tx(tbA, 32768 + 768);
-    bulk_g2s(sm + kS2_WH, rec + kOffWhi, 16384, tbA);
-    bulk_g2s(sm + kS2_WL, rec + kOffWlo, 16384, tbA);
+    bulk_g2s(sm + kS2_W, rec + kOffW, 32768, tbA);
     bulk_g2s(sm + kS2_GK, rec + kOffGK, 768, tbA);
     pend_a = ci;
   };
@@ -666,15 +668,15 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    // (c) X^T = S W^T (3 passes) -> cols [128, 192);  O1^T = S Q^T -> o1col.
+    // (c) X^T = S W^T (hi/lo: three products in two MMA groups) -> cols
+    // [128, 256), summed by the Delta step;  O1^T = S Q^T -> o1col.
     if (tid == 0) {
       const uint32_t sah = smem_u32(sm + kS2_SAH), sal = smem_u32(sm + kS2_SAL);
-      const uint32_t wh = smem_u32(sm + kS2_WH), wl = smem_u32(sm + kS2_WL);
+      const uint32_t w = smem_u32(sm + kS2_W);
       const uint32_t qt = smem_u32(sm + kS2_Q);
-      const uint32_t idw = id64 | kTransB;
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(wh, 64, kk), idw, kk > 0);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(wl, 64, kk), idw, 1);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(wh, 64, kk), idw, 1);
+      // cols [128, 192): S_hi W_hi^T + S_lo W_hi^T;  cols [192, 256): S_hi W_lo^T
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
+      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(w, 128, kk), id64 | kTransB, 1);
       mma_commit(mbar);   // X is what Delta waits for; O1 completes with the output barrier
       for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
       mma_commit(qbar);   // the Q tile may be refilled once O1 has read it
@@ -700,8 +702,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     __syncthreads();   // the output staging in the Delta^T area has been read
     // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
     {
-      float xv[32];
+      float xv[32], xl[32];
       tmem_ld32(tmem_warp_addr(taddr, 128 + 32 * hf), xv);
+      tmem_ld32(tmem_warp_addr(taddr, 192 + 32 * hf), xl);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) xv[e] += xl[e];
 #pragma unroll
       for (int e8 = 0; e8 < 4; ++e8) {
         const float4 u0 = us[row * 16 + ((8 * hf + 2 * e8) ^ (row & 7))];
