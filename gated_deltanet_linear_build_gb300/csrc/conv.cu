@@ -276,7 +276,7 @@ __device__ __forceinline__ float sel3_4(const float (&a)[3][4], int i, int ch) {
 }
 
 struct CvMeta {
-  int seq, tok, rows, pos, flags, L;
+  int seq, tok, rows, pos, flags, L, slot;
 };
 
 template <bool kSilu>
@@ -286,7 +286,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                        __nv_bfloat16* __restrict__ state, const uint8_t* __restrict__ has_init,
                        const int32_t* __restrict__ cu, const gdn_conv_chunk_t* __restrict__ chunks,
                        const int32_t* __restrict__ num_chunks, int units, int T, int C, int N,
-                       __nv_bfloat16* __restrict__ y) {
+                       __nv_bfloat16* __restrict__ y, const StateSlots slots) {
   using namespace tc;
   extern __shared__ __align__(128) unsigned char sm[];
   CvMeta* meta = reinterpret_cast<CvMeta*>(sm + kCvMetaOff);
@@ -331,7 +331,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
     for (int base = d0; base < d1 && ok; base += 32) {
       const int d = base + lane;
       int4 dd = make_int4(-1, 0, 0, 0);
-      int L = 0, init = 0;
+      int L = 0, init = 0, slot = 0;
       if (d < d1) {
         int n;
         if (chunks) {
@@ -345,6 +345,10 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
         const int seq = dd.x, tok0 = dd.y, len = dd.z, pos = dd.w;
         bool valid = d < n && seq >= 0 && seq < N && len > 0 && (pos == 0 || pos >= 3) &&
                      tok0 >= pos && (int64_t)tok0 + len <= T;
+        if (valid) {
+          slot = state_slot(slots, seq);   // padding entries are skipped
+          valid = slot >= 0;
+        }
         if (valid && pos == 0) {
           // Only the first descriptor of a sequence needs the sequence
           // length (for the new state) and the initial-state flag.
@@ -363,6 +367,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
         const int pos = __shfl_sync(0xffffffffu, dd.w, j);
         const int Lj = __shfl_sync(0xffffffffu, L, j);
         const int initj = __shfl_sync(0xffffffffu, init, j);
+        const int slotj = __shfl_sync(0xffffffffu, slot, j);
         if (seq < 0) continue;
         if (lane == 0) {
           for (int r0 = 0; r0 < len && ok; r0 += kCvRows, ++it) {
@@ -378,6 +383,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
             m.rows = min(kCvRows, len - r0);
             m.pos = pos + r0;
             m.L = Lj;
+            m.slot = slotj;
             m.flags = 0;
             unsigned char* dst = sm + st * kCvStageBytes;
             const __nv_bfloat16* xr = x + (int64_t)m.tok * x_stride + c_base;
@@ -404,7 +410,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                 bulk_g2s(dst + (kCvHalo + i) * kCvSlot, xr - (int64_t)(3 - i) * x_stride, seg,
                          full + st);
             } else if (m.flags & kHaloState) {
-              bulk_g2s(dst + kCvHalo * kCvSlot, state + ((size_t)seq * C + c_base) * 3, 3 * seg,
+              bulk_g2s(dst + kCvHalo * kCvSlot, state + ((size_t)slotj * C + c_base) * 3, 3 * seg,
                        full + st);
             }
             if (m.flags & kTailRows) {
@@ -513,7 +519,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
             ns[j][3] = bf16hi(u.y);
           }
         }
-        store_state4(state + ((size_t)m.seq * C + c0) * 3, ns);
+        store_state4(state + ((size_t)m.slot * C + c0) * 3, ns);
       }
       const unsigned char* src = stage + kCvData * kCvSlot + gt * 8;
       __nv_bfloat16* dst = y + (int64_t)m.tok * C + c0;
@@ -548,14 +554,15 @@ __global__ void __launch_bounds__(kConvThreads)
 conv_update_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                    const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ bias,
                    __nv_bfloat16* __restrict__ state, int C, int silu,
-                   __nv_bfloat16* __restrict__ y) {
+                   __nv_bfloat16* __restrict__ y, const StateSlots slots) {
   pdl_wait();
   pdl_trigger();
   const int n = blockIdx.y;
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
-  if (c0 >= C) return;
+  const int slot = state_slot(slots, n);
+  if (c0 >= C || slot < 0) return;
   float wf[4][8], bf[8], win[3][8], xc[8], out[8];
-  __nv_bfloat16* st_row = state + ((size_t)n * C + c0) * 3;
+  __nv_bfloat16* st_row = state + ((size_t)slot * C + c0) * 3;
   const uint4 xv = ldg16(x + (size_t)n * x_stride + c0);
   load_state8(st_row, win);
   load_taps(w, c0, wf);
@@ -595,7 +602,7 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
                              void* conv_state, const uint8_t* has_init, const int32_t* cu,
                              const gdn_conv_chunk_t* chunks, const int32_t* num_chunks,
                              int32_t units, int32_t T, int32_t C, int32_t N, int32_t silu,
-                             void* y, cudaStream_t st) {
+                             void* y, cudaStream_t st, StateSlots slots) {
   if (units <= 0) return GDN_OK;
   static const int num_sms = [] {
     int dev = 0, n = 0;
@@ -614,18 +621,18 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
       kern, dim3(NB * R), dim3(kCvThreads), kCvSmem, st, static_cast<const __nv_bfloat16*>(x),
       x_stride, static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(bias),
       static_cast<__nv_bfloat16*>(conv_state), has_init, cu, chunks, num_chunks, (int)units,
-      (int)T, (int)C, (int)N, static_cast<__nv_bfloat16*>(y)));
+      (int)T, (int)C, (int)N, static_cast<__nv_bfloat16*>(y), slots));
 }
 
 gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
                                 const void* bias, void* conv_state, int32_t N, int32_t C,
-                                int32_t silu, void* y, cudaStream_t st) {
+                                int32_t silu, void* y, cudaStream_t st, StateSlots slots) {
   dim3 grid((C / 8 + kConvThreads - 1) / kConvThreads, N);
   return check_launch(launch_pdl(
       conv_update_kernel, grid, dim3(kConvThreads), 0, st, static_cast<const __nv_bfloat16*>(x),
       x_stride, static_cast<const __nv_bfloat16*>(w), static_cast<const __nv_bfloat16*>(bias),
       static_cast<__nv_bfloat16*>(conv_state), (int)C, (int)silu,
-      static_cast<__nv_bfloat16*>(y)));
+      static_cast<__nv_bfloat16*>(y), slots));
 }
 
 }  // namespace gdn

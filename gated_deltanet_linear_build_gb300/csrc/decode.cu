@@ -55,7 +55,7 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
                     int64_t qk_stride, const __nv_bfloat16* __restrict__ v, int64_t v_stride,
                     const float* __restrict__ a, const float* __restrict__ b,
                     float* __restrict__ S, __nv_bfloat16* __restrict__ o, int Hk, int Hv,
-                    int qk_l2norm) {
+                    int qk_l2norm, const StateSlots slots) {
   using Cfg = DecodeCfg<DK, DV>;
   constexpr int LPR = Cfg::kLanesPerRow;
   __shared__ float s_o[DV];
@@ -64,6 +64,8 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 
   const int nh = blockIdx.x;  // n * Hv + h
   const int n = nh / Hv, h = nh - n * Hv;
+  const int slot = state_slot(slots, n);
+  if (slot < 0) return;      // a padding entry
   const int g = h / (Hv / Hk);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane % LPR;              // float4 column of this lane
@@ -81,7 +83,7 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
   const float kq = group_sum<LPR>(k4.x * q4.x + k4.y * q4.y + k4.z * q4.z + k4.w * q4.w);
   const float av = __ldg(a + nh), bv = __ldg(b + nh);
 
-  float* Sh = S + (size_t)nh * DV * DK;
+  float* Sh = S + ((size_t)slot * Hv + h) * DV * DK;
   const __nv_bfloat16* vh = v + n * v_stride + (int64_t)h * DV;
 
 #pragma unroll 1
@@ -181,6 +183,7 @@ struct DecodeArgs {
   float* S;
   __nv_bfloat16* o;
   int Hk, Hv, qk_l2norm, units;
+  StateSlots slots;   // unfused only: sequence -> state slot
 };
 
 // Sum over the 32 lanes of eight per-lane values at once (transpose-reduce):
@@ -346,8 +349,13 @@ delta_decode_stream_kernel(const DecodeArgs p) {
         } else {
           int n, h, g, part;
           unit_coords(unit, n, h, g, part);
-          mbar_arrive_expect_tx(full + st, kDecUnitBytes + 256 + 256 + 2 * kDecRows);
-          bulk_g2s(dst, p.S + (size_t)unit * kDecRows * 128, kDecUnitBytes, full + st);
+          const int slot = state_slot(p.slots, n);
+          // a padding entry: no state rows (the stage's stale rows are updated
+          // and discarded, nothing is stored)
+          mbar_arrive_expect_tx(full + st, (slot >= 0 ? kDecUnitBytes : 0) + 256 + 256 + 2 * kDecRows);
+          if (slot >= 0)
+            bulk_g2s(dst, p.S + (((size_t)slot * Hv + h) * kDecUnitsPerHead + part) * kDecRows * 128,
+                     kDecUnitBytes, full + st);
           bulk_g2s(dst + kDecOffK, p.k + n * p.qk_stride + (int64_t)g * 128, 256, full + st);
           bulk_g2s(dst + kDecOffQ, p.q + n * p.qk_stride + (int64_t)g * 128, 256, full + st);
           bulk_g2s(dst + kDecOffV, p.v + n * p.v_stride + (int64_t)h * 128 + part * kDecRows,
@@ -359,8 +367,14 @@ delta_decode_stream_kernel(const DecodeArgs p) {
         const int st = i % kDecStages;
         mbar_wait(empty + st, (i / kDecStages) & 1);
         const int unit = blockIdx.x + i * G;
-        bulk_s2g(p.S + (size_t)unit * kDecRows * 128, sm + st * kDecStageBytes, kDecUnitBytes);
-        bulk_s2g(p.o + (size_t)unit * kDecRows, sm + st * kDecStageBytes + kDecOffO, 2 * kDecRows);
+        int n, h, g, part;
+        unit_coords(unit, n, h, g, part);
+        const int slot = kFused ? n : state_slot(p.slots, n);
+        if (slot >= 0) {
+          bulk_s2g(p.S + (((size_t)slot * Hv + h) * kDecUnitsPerHead + part) * kDecRows * 128,
+                   sm + st * kDecStageBytes, kDecUnitBytes);
+          bulk_s2g(p.o + (size_t)unit * kDecRows, sm + st * kDecStageBytes + kDecOffO, 2 * kDecRows);
+        }
         bulk_commit();
         // Refill the stage stored one unit ago (its store has had a unit's
         // time to read shared memory), keeping kDecStages - 1 loads in flight.
@@ -477,24 +491,26 @@ delta_decode_stream_kernel(const DecodeArgs p) {
 template <int DK, int DV>
 gdn_status_t launch_decode_t(const void* q, const void* k, int64_t qk_stride, const void* v,
                              int64_t v_stride, const float* a, const float* b, float* S,
-                             void* o, int N, int Hk, int Hv, int qk_l2norm, cudaStream_t st) {
+                             void* o, int N, int Hk, int Hv, int qk_l2norm, cudaStream_t st,
+                             StateSlots slots) {
   using Cfg = DecodeCfg<DK, DV>;
   return check_launch(launch_pdl(
       delta_decode_kernel<DK, DV>, dim3(N * Hv), dim3(Cfg::kThreads), 0, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride,
       static_cast<const __nv_bfloat16*>(v), v_stride, a, b, S, static_cast<__nv_bfloat16*>(o),
-      Hk, Hv, qk_l2norm));
+      Hk, Hv, qk_l2norm, slots));
 }
 
 template <int DK>
 gdn_status_t launch_decode_dv(int dv, const void* q, const void* k, int64_t qk_stride,
                               const void* v, int64_t v_stride, const float* a, const float* b,
-                              float* S, void* o, int N, int Hk, int Hv, int l2, cudaStream_t st) {
+                              float* S, void* o, int N, int Hk, int Hv, int l2, cudaStream_t st,
+                              StateSlots slots) {
   switch (dv) {
-    case 16: return launch_decode_t<DK, 16>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st);
-    case 32: return launch_decode_t<DK, 32>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st);
-    case 64: return launch_decode_t<DK, 64>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st);
-    case 128: return launch_decode_t<DK, 128>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st);
+    case 16: return launch_decode_t<DK, 16>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st, slots);
+    case 32: return launch_decode_t<DK, 32>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st, slots);
+    case 64: return launch_decode_t<DK, 64>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st, slots);
+    case 128: return launch_decode_t<DK, 128>(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, l2, st, slots);
   }
   return GDN_ERR_UNSUPPORTED;
 }
@@ -552,7 +568,7 @@ gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride
                                  const void* v, int64_t v_stride, const float* a,
                                  const float* b, float* S, void* o, int32_t N, int32_t Hk,
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, StateSlots slots) {
   if (dk == 128 && dv == 128) {
     DecodeArgs p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -568,13 +584,14 @@ gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride
     p.Hv = Hv;
     p.qk_l2norm = qk_l2norm;
     p.units = N * Hv * kDecUnitsPerHead;
+    p.slots = slots;
     return launch_decode_stream<false>(p, st);
   }
   switch (dk) {
-    case 16: return launch_decode_dv<16>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st);
-    case 32: return launch_decode_dv<32>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st);
-    case 64: return launch_decode_dv<64>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st);
-    case 128: return launch_decode_dv<128>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st);
+    case 16: return launch_decode_dv<16>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
+    case 32: return launch_decode_dv<32>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
+    case 64: return launch_decode_dv<64>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
+    case 128: return launch_decode_dv<128>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
   }
   return GDN_ERR_UNSUPPORTED;
 }

@@ -71,14 +71,23 @@ static gdn_status_t check_conv_common(const void* x, int64_t x_stride, const voi
   return GDN_OK;
 }
 
-gdn_status_t gdn_causal_conv1d_fwd(const void* x, int64_t x_stride, const void* w,
-                                   const void* bias, void* conv_state,
-                                   const uint8_t* has_initial_state,
-                                   const int32_t* cu_seqlens,
-                                   const gdn_conv_chunk_t* chunks,
-                                   const int32_t* num_chunks, int32_t max_chunks,
-                                   int32_t T, int32_t C, int32_t K, int32_t N,
-                                   int32_t silu, void* y, void* stream) {
+// The state-slot argument pair of the *_slots entry points: a device array of
+// N slot numbers and the number of slots in the state cache.
+static gdn_status_t make_slots(const int32_t* state_indices, int32_t num_slots,
+                               StateSlots* out) {
+  if (!state_indices || num_slots < 0) return GDN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(state_indices) & 3u) != 0) return GDN_ERR_ALIGNMENT;
+  out->idx = state_indices;
+  out->count = num_slots;
+  return GDN_OK;
+}
+
+static gdn_status_t conv_fwd_impl(const void* x, int64_t x_stride, const void* w,
+                                  const void* bias, void* conv_state,
+                                  const uint8_t* has_initial_state, const int32_t* cu_seqlens,
+                                  const gdn_conv_chunk_t* chunks, const int32_t* num_chunks,
+                                  int32_t max_chunks, int32_t T, int32_t C, int32_t K, int32_t N,
+                                  int32_t silu, void* y, void* stream, StateSlots slots) {
   if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
   if ((chunks == nullptr) != (num_chunks == nullptr)) return GDN_ERR_INVALID_ARG;
   if (chunks && max_chunks < 0) return GDN_ERR_INVALID_ARG;
@@ -89,19 +98,68 @@ gdn_status_t gdn_causal_conv1d_fwd(const void* x, int64_t x_stride, const void* 
   if (chunks && !aligned16(chunks)) return GDN_ERR_ALIGNMENT;
   const int32_t units = chunks ? max_chunks : N;
   return launch_conv_fwd(x, x_stride, w, bias, conv_state, has_initial_state, cu_seqlens, chunks,
-                         num_chunks, units, T, C, N, silu, y, static_cast<cudaStream_t>(stream));
+                         num_chunks, units, T, C, N, silu, y, static_cast<cudaStream_t>(stream),
+                         slots);
+}
+
+gdn_status_t gdn_causal_conv1d_fwd(const void* x, int64_t x_stride, const void* w,
+                                   const void* bias, void* conv_state,
+                                   const uint8_t* has_initial_state,
+                                   const int32_t* cu_seqlens,
+                                   const gdn_conv_chunk_t* chunks,
+                                   const int32_t* num_chunks, int32_t max_chunks,
+                                   int32_t T, int32_t C, int32_t K, int32_t N,
+                                   int32_t silu, void* y, void* stream) {
+  return conv_fwd_impl(x, x_stride, w, bias, conv_state, has_initial_state, cu_seqlens, chunks,
+                       num_chunks, max_chunks, T, C, K, N, silu, y, stream, StateSlots{});
+}
+
+gdn_status_t gdn_causal_conv1d_fwd_slots(const void* x, int64_t x_stride, const void* w,
+                                         const void* bias, void* conv_state,
+                                         const uint8_t* has_initial_state,
+                                         const int32_t* cu_seqlens,
+                                         const gdn_conv_chunk_t* chunks,
+                                         const int32_t* num_chunks, int32_t max_chunks,
+                                         int32_t T, int32_t C, int32_t K, int32_t N,
+                                         int32_t silu, void* y,
+                                         const int32_t* state_indices, int32_t num_slots,
+                                         void* stream) {
+  StateSlots slots;
+  gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
+  if (rc != GDN_OK) return rc;
+  return conv_fwd_impl(x, x_stride, w, bias, conv_state, has_initial_state, cu_seqlens, chunks,
+                       num_chunks, max_chunks, T, C, K, N, silu, y, stream, slots);
+}
+
+static gdn_status_t conv_update_impl(const void* x, int64_t x_stride, const void* w,
+                                     const void* bias, void* conv_state, int32_t N, int32_t C,
+                                     int32_t K, int32_t silu, void* y, void* stream,
+                                     StateSlots slots) {
+  if (N < 0) return GDN_ERR_INVALID_ARG;
+  if (N == 0) return GDN_OK;
+  gdn_status_t rc = check_conv_common(x, x_stride, w, bias, conv_state, C, K, silu, y);
+  if (rc != GDN_OK) return rc;
+  return launch_conv_update(x, x_stride, w, bias, conv_state, N, C, silu, y,
+                            static_cast<cudaStream_t>(stream), slots);
 }
 
 gdn_status_t gdn_causal_conv1d_update(const void* x, int64_t x_stride, const void* w,
                                       const void* bias, void* conv_state, int32_t N,
                                       int32_t C, int32_t K, int32_t silu, void* y,
                                       void* stream) {
-  if (N < 0) return GDN_ERR_INVALID_ARG;
-  if (N == 0) return GDN_OK;
-  gdn_status_t rc = check_conv_common(x, x_stride, w, bias, conv_state, C, K, silu, y);
+  return conv_update_impl(x, x_stride, w, bias, conv_state, N, C, K, silu, y, stream,
+                          StateSlots{});
+}
+
+gdn_status_t gdn_causal_conv1d_update_slots(const void* x, int64_t x_stride, const void* w,
+                                            const void* bias, void* conv_state, int32_t N,
+                                            int32_t C, int32_t K, int32_t silu, void* y,
+                                            const int32_t* state_indices, int32_t num_slots,
+                                            void* stream) {
+  StateSlots slots;
+  gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
   if (rc != GDN_OK) return rc;
-  return launch_conv_update(x, x_stride, w, bias, conv_state, N, C, silu, y,
-                            static_cast<cudaStream_t>(stream));
+  return conv_update_impl(x, x_stride, w, bias, conv_state, N, C, K, silu, y, stream, slots);
 }
 
 static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_stride,
@@ -120,11 +178,10 @@ static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_
   return GDN_OK;
 }
 
-gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stride,
-                                   const void* v, int64_t v_stride, const float* a,
-                                   const float* b, float* S, void* o, int32_t N,
-                                   int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                   int32_t qk_l2norm, void* stream) {
+static gdn_status_t decode_impl(const void* q, const void* k, int64_t qk_stride, const void* v,
+                                int64_t v_stride, const float* a, const float* b, float* S,
+                                void* o, int32_t N, int32_t Hk, int32_t Hv, int32_t dk,
+                                int32_t dv, int32_t qk_l2norm, void* stream, StateSlots slots) {
   if (N < 0) return GDN_ERR_INVALID_ARG;
   if (N == 0) return GDN_OK;
   gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
@@ -132,7 +189,29 @@ gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stri
   if (rc != GDN_OK) return rc;
   if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
   return launch_delta_decode(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv,
-                             qk_l2norm, static_cast<cudaStream_t>(stream));
+                             qk_l2norm, static_cast<cudaStream_t>(stream), slots);
+}
+
+gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stride,
+                                   const void* v, int64_t v_stride, const float* a,
+                                   const float* b, float* S, void* o, int32_t N,
+                                   int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                   int32_t qk_l2norm, void* stream) {
+  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, qk_l2norm,
+                     stream, StateSlots{});
+}
+
+gdn_status_t gdn_delta_rule_decode_slots(const void* q, const void* k, int64_t qk_stride,
+                                         const void* v, int64_t v_stride, const float* a,
+                                         const float* b, float* S, void* o, int32_t N,
+                                         int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                         int32_t qk_l2norm, const int32_t* state_indices,
+                                         int32_t num_slots, void* stream) {
+  StateSlots slots;
+  gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
+  if (rc != GDN_OK) return rc;
+  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, qk_l2norm,
+                     stream, slots);
 }
 
 gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* w,
@@ -169,15 +248,13 @@ size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv, i
   return prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
 }
 
-gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
-                                            const void* v, int64_t v_stride,
-                                            const float* a, const float* b,
-                                            const int32_t* cu_seqlens, int32_t N, int32_t T,
-                                            float* S, const uint8_t* has_initial_state,
-                                            void* o, int32_t Hk, int32_t Hv, int32_t dk,
-                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
-                                            void* workspace, size_t workspace_bytes,
-                                            void* stream) {
+static gdn_status_t prefill_impl(const void* q, const void* k, int64_t qk_stride,
+                                 const void* v, int64_t v_stride, const float* a, const float* b,
+                                 const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
+                                 const uint8_t* has_initial_state, void* o, int32_t Hk,
+                                 int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
+                                 int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+                                 void* stream, StateSlots slots) {
   if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
   if (chunk != 64) return GDN_ERR_UNSUPPORTED;
   if (T == 0 || N == 0) return GDN_OK;
@@ -191,7 +268,35 @@ gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
   return launch_delta_prefill(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
                               has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
-                              static_cast<cudaStream_t>(stream));
+                              static_cast<cudaStream_t>(stream), slots);
+}
+
+gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
+                                            const void* v, int64_t v_stride,
+                                            const float* a, const float* b,
+                                            const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                            float* S, const uint8_t* has_initial_state,
+                                            void* o, int32_t Hk, int32_t Hv, int32_t dk,
+                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
+                                            void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  return prefill_impl(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
+                      has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                      workspace_bytes, stream, StateSlots{});
+}
+
+gdn_status_t gdn_delta_rule_prefill_chunked_slots(
+    const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
+    const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
+    const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+    int32_t chunk, int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+    const int32_t* state_indices, int32_t num_slots, void* stream) {
+  StateSlots slots;
+  gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
+  if (rc != GDN_OK) return rc;
+  return prefill_impl(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
+                      has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                      workspace_bytes, stream, slots);
 }
 
 }  // extern "C"

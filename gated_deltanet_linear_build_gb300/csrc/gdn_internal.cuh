@@ -163,6 +163,23 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ---------------------------------------------------------------------------
+// Optional indirection from a sequence to its state slot: serving engines keep
+// conv_state and S in a cache of slots and pass, per call, the slot of each
+// sequence. idx == nullptr: the slot is the sequence index. A slot outside
+// [0, count) marks a sequence whose state is not touched and whose outputs are
+// not written (a padding entry).
+// ---------------------------------------------------------------------------
+struct StateSlots {
+  const int32_t* idx = nullptr;
+  int32_t count = 0;
+};
+__device__ __forceinline__ int state_slot(const StateSlots& s, int n) {
+  if (s.idx == nullptr) return n;
+  const int v = __ldg(s.idx + n);
+  return (v >= 0 && v < s.count) ? v : -1;
+}
+
 // Launchers implemented in the kernel translation units. They assume their
 // arguments were validated by the C ABI layer.
 gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
@@ -173,17 +190,17 @@ gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, con
                              void* conv_state, const uint8_t* has_init, const int32_t* cu,
                              const gdn_conv_chunk_t* chunks, const int32_t* num_chunks,
                              int32_t units, int32_t T, int32_t C, int32_t N, int32_t silu,
-                             void* y, cudaStream_t st);
+                             void* y, cudaStream_t st, StateSlots slots = {});
 
 gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
                                 const void* bias, void* conv_state, int32_t N, int32_t C,
-                                int32_t silu, void* y, cudaStream_t st);
+                                int32_t silu, void* y, cudaStream_t st, StateSlots slots = {});
 
 gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride,
                                  const void* v, int64_t v_stride, const float* a,
                                  const float* b, float* S, void* o, int32_t N, int32_t Hk,
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
-                                 cudaStream_t st);
+                                 cudaStream_t st, StateSlots slots = {});
 
 // Conv update and delta-rule decode in one launch (dk = dv = 128).
 gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
@@ -200,7 +217,8 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
                                   const float* b, const int32_t* cu, int32_t N, int32_t T,
                                   float* S, const uint8_t* has_init, void* o, int32_t Hk,
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
-                                  int32_t qk_l2norm, void* workspace, cudaStream_t st);
+                                  int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                                  StateSlots slots = {});
 
 // Tensor-core (tcgen05) chunked prefill for dk = dv = 128.
 size_t prefill_tc_workspace_bytes(int32_t T, int32_t N, int32_t Hv);
@@ -208,6 +226,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
                                int64_t v_stride, const float* a, const float* b,
                                const int32_t* cu, int32_t N, int32_t T, float* S,
                                const uint8_t* has_init, void* o, int32_t Hk, int32_t Hv,
-                               int32_t qk_l2norm, void* workspace, cudaStream_t st);
+                               int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                               StateSlots slots = {});
 
 }  // namespace gdn

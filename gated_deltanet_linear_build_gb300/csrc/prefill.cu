@@ -178,7 +178,7 @@ state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   float* __restrict__ S, const uint8_t* __restrict__ has_init,
                   __nv_bfloat16* __restrict__ o, int Hk, int Hv, int qk_l2norm,
                   const float* __restrict__ g_ws, const float* __restrict__ w_ws,
-                  const float* __restrict__ u_ws) {
+                  const float* __restrict__ u_ws, const StateSlots slots) {
   constexpr int PK = DK + 1, PT = kChunk + 1, PS = SL + 1;
   extern __shared__ float smem[];
   float* Ss = smem;                  // [SL][PK]   state rows i (slice), columns j
@@ -195,7 +195,9 @@ state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   const int tid = threadIdx.x;
   const int start = cu[seq], end = cu[seq + 1];
   if (end <= start || start < 0 || end > T) return;
-  float* Sg = S + ((size_t)seq * Hv + h) * DV * DK + (size_t)i0 * DK;
+  const int slot = state_slot(slots, seq);
+  if (slot < 0) return;   // a padding entry: state and outputs untouched
+  float* Sg = S + ((size_t)slot * Hv + h) * DV * DK + (size_t)i0 * DK;
   const bool init = has_init != nullptr && has_init[seq] != 0;
   for (int idx = tid; idx < SL * DK; idx += kThreads) {
     const int i = idx / DK, j = idx % DK;
@@ -270,7 +272,7 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
                               int64_t v_stride, const float* a, const float* b,
                               const int32_t* cu, int N, int T, float* S,
                               const uint8_t* has_init, void* o, int Hk, int Hv, int l2,
-                              void* workspace, cudaStream_t st) {
+                              void* workspace, cudaStream_t st, StateSlots slots) {
   constexpr int DK = D, DV = D, SL = D < kSlice ? D : kSlice;
   const WsLayout L = ws_layout(T, N, Hv, DK, DV);
   char* ws = static_cast<char*>(workspace);
@@ -309,7 +311,7 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   if ((rc = check_launch()) != GDN_OK) return rc;
   k2<<<dim3(N, Hv, DV / SL), kThreads, smem2, st>>>(qp, kp, qk_stride, cu, T, S, has_init,
                                                     static_cast<__nv_bfloat16*>(o), Hk, Hv, l2,
-                                                    g_ws, w_ws, u_ws);
+                                                    g_ws, w_ws, u_ws, slots);
   return check_launch();
 }
 
@@ -327,14 +329,15 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
                                   const float* b, const int32_t* cu, int32_t N, int32_t T,
                                   float* S, const uint8_t* has_init, void* o, int32_t Hk,
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
-                                  int32_t qk_l2norm, void* workspace, cudaStream_t st) {
+                                  int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                                  StateSlots slots) {
   (void)chunk;
   if (dk != dv) return GDN_ERR_UNSUPPORTED;
   switch (dk) {
-    case 16: return launch_prefill_t<16>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
-    case 32: return launch_prefill_t<32>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
-    case 64: return launch_prefill_t<64>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
-    case 128: return launch_prefill_tc(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st);
+    case 16: return launch_prefill_t<16>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
+    case 32: return launch_prefill_t<32>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
+    case 64: return launch_prefill_t<64>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
+    case 128: return launch_prefill_tc(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
   }
   return GDN_ERR_UNSUPPORTED;
 }

@@ -471,7 +471,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                 int64_t qk_stride, const int32_t* __restrict__ cu, int T, int Hk,
                 float* __restrict__ S, const uint8_t* __restrict__ has_init,
                 __nv_bfloat16* __restrict__ o, int Hv, const unsigned char* __restrict__ records,
-                int32_t* __restrict__ hdr) {
+                int32_t* __restrict__ hdr, const StateSlots slots) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const float* gk = reinterpret_cast<const float*>(sm + kS2_GK);
   const float4* us = reinterpret_cast<const float4*>(sm + kS2_U);
@@ -495,6 +495,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   pdl_trigger();
   const int start = cu[seq], end = cu[seq + 1];
   if (start < 0 || end <= start || end > T) return;
+  const int sslot = state_slot(slots, seq);
+  if (sslot < 0) return;   // a padding entry: state and outputs untouched
   const int nchunks = (end - start + kC - 1) / kC;
 
   if (tid == 0) {
@@ -527,7 +529,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   const int first = *s_first;
   const bool records_ok = first + nchunks <= hdr[0];
 
-  float* Sg = S + (((size_t)seq * Hv + h) * kD + row) * kD;
+  float* Sg = S + (((size_t)sslot * Hv + h) * kD + row) * kD;
   const bool init = has_init != nullptr && has_init[seq] != 0;
 #pragma unroll
   for (int blk = 0; blk < 2; ++blk) {
@@ -808,7 +810,8 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
                                int64_t v_stride, const float* a, const float* b,
                                const int32_t* cu, int32_t N, int32_t T, float* S,
                                const uint8_t* has_init, void* o, int32_t Hk, int32_t Hv,
-                               int32_t qk_l2norm, void* workspace, cudaStream_t st) {
+                               int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                               StateSlots slots) {
   const TcLayout L = tc_layout(T, N, Hv);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   int32_t* hdr = reinterpret_cast<int32_t*>(ws);
@@ -833,7 +836,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
       tc_state_kernel, dim3(N, Hv), dim3(kThreads2), kS2_BYTES, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride, cu,
       T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, (const unsigned char*)records,
-      hdr));
+      hdr, slots));
 }
 
 }  // namespace gdn

@@ -33,6 +33,10 @@ EXPORTED_SYMBOLS = (
     "gdn_delta_rule_prefill_workspace_size",
     "gdn_delta_rule_prefill_chunked",
     "gdn_delta_rule_prefill_chunked_noalloc",
+    "gdn_causal_conv1d_fwd_slots",
+    "gdn_causal_conv1d_update_slots",
+    "gdn_delta_rule_decode_slots",
+    "gdn_delta_rule_prefill_chunked_slots",
     "gdn_status_string",
     "gdn_last_cuda_error_string",
 )
@@ -70,6 +74,17 @@ _SIGNATURES = {
     "gdn_delta_rule_prefill_chunked_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P,
                                                               _I32, _I32, _P, _P, _P, _I32, _I32,
                                                               _I32, _I32, _I32, _I32, _P]),
+    "gdn_causal_conv1d_fwd_slots": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _I32,
+                                                   _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
+                                                   _P]),
+    "gdn_causal_conv1d_update_slots": (ctypes.c_int, [_P, _I64, _P, _P, _P, _I32, _I32, _I32,
+                                                      _I32, _P, _P, _I32, _P]),
+    "gdn_delta_rule_decode_slots": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _P, _I32,
+                                                   _I32, _I32, _I32, _I32, _I32, _P, _I32, _P]),
+    "gdn_delta_rule_prefill_chunked_slots": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P,
+                                                            _I32, _I32, _P, _P, _P, _I32, _I32,
+                                                            _I32, _I32, _I32, _I32, _P,
+                                                            ctypes.c_size_t, _P, _I32, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_cuda_error_string": (ctypes.c_char_p, []),
 }
@@ -220,6 +235,67 @@ def delta_rule_prefill_chunked_noalloc(q, k, v, a, b, cu_seqlens, S, has_initial
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
         chunk, int(qk_l2norm), _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked_noalloc")
+
+
+# ----------------------------------------------------------------------------
+# State-slot variants: conv_state [num_slots, C, 3] and S [num_slots, Hv, dv, dk]
+# form a cache; sequence n of the batch uses slot state_indices[n] (device
+# int32 [N]); an index outside [0, num_slots) is a padding entry whose state
+# and outputs are left untouched. num_slots defaults to the cache's first
+# dimension.
+# ----------------------------------------------------------------------------
+
+def causal_conv1d_fwd_slots(x, w, bias, conv_state, has_initial_state, cu_seqlens, y,
+                            state_indices, *, num_slots=None, chunks=None, num_chunks=None,
+                            silu: bool = True, stream=None):
+    T, C = x.shape
+    N = cu_seqlens.numel() - 1
+    ns = conv_state.shape[0] if num_slots is None else num_slots
+    rc = _lib().gdn_causal_conv1d_fwd_slots(
+        _ptr(x), x.stride(0), _ptr(w), _ptr(bias), _ptr(conv_state), _ptr(has_initial_state),
+        _ptr(cu_seqlens), _ptr(chunks), _ptr(num_chunks),
+        chunks.shape[0] if chunks is not None else 0, T, C, w.shape[1], N, int(silu), _ptr(y),
+        _ptr(state_indices), ns, _stream(stream))
+    _check(rc, "gdn_causal_conv1d_fwd_slots")
+
+
+def causal_conv1d_update_slots(x, w, bias, conv_state, y, state_indices, *, num_slots=None,
+                               silu: bool = True, stream=None):
+    N, C = x.shape
+    ns = conv_state.shape[0] if num_slots is None else num_slots
+    rc = _lib().gdn_causal_conv1d_update_slots(_ptr(x), x.stride(0), _ptr(w), _ptr(bias),
+                                               _ptr(conv_state), N, C, w.shape[1], int(silu),
+                                               _ptr(y), _ptr(state_indices), ns, _stream(stream))
+    _check(rc, "gdn_causal_conv1d_update_slots")
+
+
+def delta_rule_decode_slots(q, k, v, a, b, S, o, state_indices, *, num_slots=None,
+                            qk_l2norm: bool = False, stream=None):
+    N, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    assert k.stride(0) == q.stride(0), "q and k share one token stride"
+    ns = S.shape[0] if num_slots is None else num_slots
+    rc = _lib().gdn_delta_rule_decode_slots(_ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0),
+                                            _ptr(a), _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk,
+                                            dv, int(qk_l2norm), _ptr(state_indices), ns,
+                                            _stream(stream))
+    _check(rc, "gdn_delta_rule_decode_slots")
+
+
+def delta_rule_prefill_chunked_slots(q, k, v, a, b, cu_seqlens, S, has_initial_state, o,
+                                     workspace, state_indices, *, num_slots=None,
+                                     chunk: int = 64, qk_l2norm: bool = False, stream=None):
+    T, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    assert k.stride(0) == q.stride(0), "q and k share one token stride"
+    ns = S.shape[0] if num_slots is None else num_slots
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib().gdn_delta_rule_prefill_chunked_slots(
+        _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
+        _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
+        chunk, int(qk_l2norm), _ptr(workspace), nbytes, _ptr(state_indices), ns, _stream(stream))
+    _check(rc, "gdn_delta_rule_prefill_chunked_slots")
 
 
 def status_string(status: int) -> str:

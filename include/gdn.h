@@ -292,6 +292,62 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
     int32_t chunk, int32_t qk_l2norm, void* stream);
 
+/*
+ * State-slot variants. Source: "RTX 5070 Ti: close Qwen3.5-4B TTFT, TPOT, and
+ * VRAM gaps vs vLLM", Problem (the serving engine runs 32 concurrent requests
+ * out of a fixed block cache); the pages do not describe the cache layout, so this is
+ * the plainest form of it: the recurrent states live in a cache of slots that
+ * outlives any one batch, and each call says which slot every sequence of the
+ * batch owns.
+ *
+ * Each *_slots call computes exactly what the call without the suffix computes,
+ * with two changes:
+ *   conv_state  BF16 [num_slots, C, 3] and S float32 [num_slots, Hv, dv, dk]:
+ *               sequence n of the batch reads and writes slot state_indices[n]
+ *               instead of entry n.
+ *   state_indices  device int32 [N], 4-byte aligned. An index outside
+ *               [0, num_slots) (for example -1) marks a padding entry: its
+ *               state is neither read nor written and its outputs (its rows of
+ *               y or o) are left as they were. The valid indices of one call
+ *               must be distinct (two sequences in one slot race); this is not
+ *               checked. has_initial_state stays indexed by sequence n.
+ *   num_slots   >= 0 (0: every entry is padding).
+ * NULL state_indices or negative num_slots is GDN_ERR_INVALID_ARG, a
+ * misaligned state_indices GDN_ERR_ALIGNMENT. The results for a valid entry
+ * are bit-identical to the call without the suffix on the gathered states.
+ */
+GDN_API gdn_status_t gdn_causal_conv1d_fwd_slots(const void* x, int64_t x_stride, const void* w,
+                                         const void* bias, void* conv_state,
+                                         const uint8_t* has_initial_state,
+                                         const int32_t* cu_seqlens,
+                                         const gdn_conv_chunk_t* chunks,
+                                         const int32_t* num_chunks, int32_t max_chunks,
+                                         int32_t T, int32_t C, int32_t K, int32_t N,
+                                         int32_t silu, void* y,
+                                         const int32_t* state_indices, int32_t num_slots,
+                                         void* stream);
+
+GDN_API gdn_status_t gdn_causal_conv1d_update_slots(const void* x, int64_t x_stride,
+                                            const void* w, const void* bias,
+                                            void* conv_state, int32_t N, int32_t C,
+                                            int32_t K, int32_t silu, void* y,
+                                            const int32_t* state_indices, int32_t num_slots,
+                                            void* stream);
+
+GDN_API gdn_status_t gdn_delta_rule_decode_slots(const void* q, const void* k, int64_t qk_stride,
+                                         const void* v, int64_t v_stride, const float* a,
+                                         const float* b, float* S, void* o, int32_t N,
+                                         int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                         int32_t qk_l2norm, const int32_t* state_indices,
+                                         int32_t num_slots, void* stream);
+
+GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_slots(
+    const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
+    const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
+    const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+    int32_t chunk, int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+    const int32_t* state_indices, int32_t num_slots, void* stream);
+
 /* Static description of a status code (never NULL). */
 GDN_API const char* gdn_status_string(gdn_status_t status);
 

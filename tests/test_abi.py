@@ -167,3 +167,47 @@ def test_decode_step_fused_validation(lib):
     assert call(x=A8) == ALIGN
     assert call(bias=A8) == ALIGN
     assert call(so=s_out + 8) == ALIGN
+
+
+def test_state_slot_variants_validation(lib):
+    """The *_slots entry points check their slot arguments first, then the
+    arguments of the call they extend; nothing launches."""
+    conv_args = [A16, 64, A16, None, A16, None, A16, None, None, 0, 18, 64, 4, 2, 1, A16]
+    f = lib.gdn_causal_conv1d_fwd_slots
+    assert f(*conv_args, None, 4, None) == INVALID                  # no state_indices
+    assert f(*conv_args, A16, -1, None) == INVALID                  # negative slot count
+    assert f(*conv_args, A16 + 2, 4, None) == ALIGN                 # int32 alignment
+    bad = list(conv_args)
+    bad[0] = A8
+    assert f(*bad, A16, 4, None) == ALIGN                           # the base check still runs
+    bad = list(conv_args)
+    bad[10] = 0
+    assert f(*bad, A16, 4, None) == OK                              # T == 0: nothing to do
+
+    g = lib.gdn_causal_conv1d_update_slots
+    assert g(A16, 64, A16, None, A16, 2, 64, 4, 1, A16, None, 4, None) == INVALID
+    assert g(A16, 64, A16, None, A16, 2, 64, 5, 1, A16, A16, 4, None) == UNSUPPORTED
+    assert g(A16, 64, A16, None, A16, 0, 64, 4, 1, A16, A16, 0, None) == OK
+
+    dec = [A16, A16, 4096, A16, 4096, A16, A16, A16, A16, 32, 16, 32, 128, 128, 0]
+    h = lib.gdn_delta_rule_decode_slots
+    assert h(*dec, None, 32, None) == INVALID
+    assert h(*dec, A16 + 1, 32, None) == ALIGN
+    bad = list(dec)
+    bad[12] = 96
+    assert h(*bad, A16, 32, None) == UNSUPPORTED
+    bad = list(dec)
+    bad[9] = 0
+    assert h(*bad, A16, 32, None) == OK
+
+    pre = [A16, A16, 4096, A16, 4096, A16, A16, A16, 2, 2048, A16, None, A16, 16, 32, 128, 128,
+           64, 0, A16 * 16, 1 << 40]
+    p = lib.gdn_delta_rule_prefill_chunked_slots
+    assert p(*pre, None, 8, None) == INVALID
+    assert p(*pre, A16, -3, None) == INVALID
+    bad = list(pre)
+    bad[20] = 16
+    assert p(*bad, A16, 8, None) == WORKSPACE
+    bad = list(pre)
+    bad[9] = 0
+    assert p(*bad, A16, 8, None) == OK
