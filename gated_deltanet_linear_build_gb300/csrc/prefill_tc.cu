@@ -438,33 +438,38 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 }
 
 // ---------------------------------------------------------------------------
-// State kernel: 256 threads. Warp w reads TMEM lanes 32 (w % 4) .. + 31 (row
-// i = lane of that quarter) and handles column half w / 4 of every row-wise
-// step, so each step is split over two warps per row.
-// TMEM: S in columns [0, 128), X^T in [128, 256) (two partial sums), O1^T and
-// O2^T double-buffered
-// in [256, 384) and [384, 512): a chunk's outputs are written back while the
-// next chunk's first MMA round runs.
-// Per chunk, the record arrives in three bulk copies issued as soon as the
-// buffer they refill is free (W and gates after the first MMA round, U after
-// Delta, P after the second round), and the raw Q and K rows of the next chunk
-// in 16-byte asynchronous copies as soon as their tiles are free.
+// State kernel: one CTA per (sequence, v-head), S [dv = 128 x dk = 128]
+// float32 resident in TMEM, chunks in order. Three warp roles hand work to
+// each other through mbarriers only, so that no role waits for another's
+// instruction stream:
+//   warps 0-7 (rows): warp w owns TMEM lanes 32 (w % 4) .. + 31 (row i of S)
+//     and column half w / 4. Per chunk: S -> BF16 hi/lo A tiles and
+//     S <- e^{g_last} S; the previous chunk's outputs; Delta = U - X.
+//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1^T = S Q^T once
+//     the S tiles are ready; S += (Delta^T D) K (hi/lo) and O2^T = Delta^T P^T
+//     once Delta is.
+//   warp 9: the next chunk's record (W and gates, U, P: bulk copies) and raw Q
+//     and K rows (16-byte asynchronous copies by all lanes), each as soon as
+//     the buffer it refills is free.
+// TMEM: S [0, 128), X^T [128, 256) (two partial sums), O1^T and O2^T
+// double-buffered in [256, 384) and [384, 512).
 // ---------------------------------------------------------------------------
-constexpr int kThreads2 = 256;
-constexpr int kS2_SAH = 0;          // S hi  [128 i][128 j]   32768
-constexpr int kS2_SAL = 32768;      // S lo                   32768
-constexpr int kS2_DA = 65536;       // Delta^T [128 i][64 s]  16384
-constexpr int kS2_DDH = 81920;      // (Delta^T D) hi         16384
-constexpr int kS2_DDL = 98304;      // (Delta^T D) lo         16384
-constexpr int kS2_Q = 114688;       // Q rows [64 r][128 j] K-major B   16384
-constexpr int kS2_K = 131072;       // K rows [64 s][128 j] (MN-major B) 16384
+constexpr int kThreads2 = 320;
+constexpr int kRowThreads = 256;
+constexpr int kS2_SAH = 0;          // S hi  [128 i][128 j]                   32768
+constexpr int kS2_SAL = 32768;      // S lo                                   32768
+constexpr int kS2_DA = 65536;       // Delta^T [128 i][64 s]; output staging  16384
+constexpr int kS2_DDH = 81920;      // (Delta^T D) hi                         16384
+constexpr int kS2_DDL = 98304;      // (Delta^T D) lo                         16384
+constexpr int kS2_Q = 114688;       // Q rows [64 r][128 j] K-major B         16384
+constexpr int kS2_K = 131072;       // K rows [64 s][128 j] (MN-major B)      16384
 constexpr int kS2_R = 147456;       // the chunk's record
 constexpr int kS2_W = kS2_R + kOffW, kS2_P = kS2_R + kOffP;
 constexpr int kS2_U = kS2_R + kOffU, kS2_GK = kS2_R + kOffGK;
 constexpr int kS2_QS = kS2_R + kRecBytes;         // e^{g_r} rq_r, two chunks [2][64]
-constexpr int kS2_DK = kS2_QS + 512;              // e^{g_last - g_s} rk_s [64]
-constexpr int kS2_BAR = kS2_DK + 256;             // barriers, TMEM slot, ...
-constexpr int kS2_BYTES = kS2_BAR + 64;
+constexpr int kS2_DK = kS2_QS + 512;              // e^{g_last - g_s} rk_s, two chunks [2][64]
+constexpr int kS2_BAR = kS2_DK + 512;             // barriers, TMEM slot, flags
+constexpr int kS2_BYTES = kS2_BAR + 128;
 
 __global__ void __launch_bounds__(kThreads2, 1)
 tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -477,20 +482,26 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   const float4* us = reinterpret_cast<const float4*>(sm + kS2_U);
   float* qs = reinterpret_cast<float*>(sm + kS2_QS);
   float* dks = reinterpret_cast<float*>(sm + kS2_DK);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kS2_BAR);
-  uint64_t* tbA = mbar + 1;   // W hi/lo + gates
-  uint64_t* tbU = mbar + 2;   // U
-  uint64_t* tbB = mbar + 3;   // P
-  uint64_t* obar = mbar + 4;  // a chunk's output MMAs (O1 and O2)
-  uint64_t* qbar = mbar + 7;  // a chunk's O1 MMAs: the Q tile is free again
-  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 40);
-  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 44);
-  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 48);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kS2_BAR);
+  uint64_t* bW = bars + 0;    // W and gates landed        (bulk copy)
+  uint64_t* bU = bars + 1;    // U landed                  (bulk copy)
+  uint64_t* bP = bars + 2;    // P landed                  (bulk copy)
+  uint64_t* bQ = bars + 3;    // Q rows landed             (32 loader lanes)
+  uint64_t* bK = bars + 4;    // K rows landed             (32 loader lanes)
+  uint64_t* bSr = bars + 5;   // S tiles written, S rescaled (256 row threads)
+  uint64_t* bDr = bars + 6;   // Delta tiles written       (256 row threads)
+  uint64_t* bX = bars + 7;    // X MMAs done               (commit)
+  uint64_t* bO1 = bars + 8;   // O1 MMAs done              (commit)
+  uint64_t* bS = bars + 9;    // S update done             (commit)
+  uint64_t* bO = bars + 10;   // O2 MMAs (and all before) done (commit)
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 96);
+  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 100);
+  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 104);
 
   const int seq = blockIdx.x, h = blockIdx.y, gh = h / (Hv / Hk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = 32 * (warp & 3) + lane;   // S row (dv index) = TMEM lane
-  const int hf = warp >> 2;                 // column / token half
+  const int row = 32 * (warp & 3) + lane;   // row warps: S row (dv index) = TMEM lane
+  const int hf = (warp >> 2) & 1;           // row warps: column / token half
   pdl_wait();
   pdl_trigger();
   const int start = cu[seq], end = cu[seq + 1];
@@ -502,12 +513,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   if (tid == 0) {
     *s_first = 0;
     *s_fail = 0;
-    mbar_init(mbar, 1);
-    mbar_init(tbA, 1);
-    mbar_init(tbU, 1);
-    mbar_init(tbB, 1);
-    mbar_init(obar, 1);
-    mbar_init(qbar, 1);
+    for (int i = 0; i < 11; ++i) {
+      const bool rows_in = bars + i == bQ || bars + i == bK;
+      const bool rows_out = bars + i == bSr || bars + i == bDr;
+      mbar_init(bars + i, rows_in ? 32u : (rows_out ? (uint32_t)kRowThreads : 1u));
+    }
   }
   __syncthreads();
   {
@@ -528,273 +538,300 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   const uint32_t taddr = *slot;
   const int first = *s_first;
   const bool records_ok = first + nchunks <= hdr[0];
-
   float* Sg = S + (((size_t)sslot * Hv + h) * kD + row) * kD;
-  const bool init = has_init != nullptr && has_init[seq] != 0;
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-    const int c0 = 64 * hf + 32 * blk;
-    float vbuf[32];
-#pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      const float4 f4 = init ? *reinterpret_cast<const float4*>(Sg + c0 + e)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      vbuf[e] = f4.x; vbuf[e + 1] = f4.y; vbuf[e + 2] = f4.z; vbuf[e + 3] = f4.w;
-    }
-    tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
-  }
 
+  // Wait for the phase of parity `par`. Returns false at once when the CTA is
+  // aborting, and starts the abort after about two seconds; the roles then
+  // run their remaining steps without waiting, so that every named barrier
+  // is still reached by all of its threads.
+  auto wait = [&](uint64_t* b, uint32_t par) -> bool {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(b, par)) {
+      if (*reinterpret_cast<volatile int*>(s_fail)) return false;
+      if (clock64() - t0 > 4000000000LL) {
+        atomicExch(s_fail, 1);
+        return false;
+      }
+    }
+    return true;
+  };
+  auto failed = [&]() { return *reinterpret_cast<volatile int*>(s_fail) != 0; };
   auto rec_of = [&](int ci) {
     return records + ((size_t)(first + ci) * Hv + h) * kRecBytes;
   };
-  // Outstanding record copies (thread 0's view), for the bounded drain on exit.
-  int pend_a = -1, pend_u = -1, pend_b = -1;
-  int pend_q = -1, pend_o = -1;   // MMA commits not yet waited for by thread 0
-  auto copy_a = [&](int ci) {
-    const unsigned char* rec = rec_of(ci);
-    mbar_arrive_expect_tx(tbA, 32768 + 768);
-    bulk_g2s(sm + kS2_W, rec + kOffW, 32768, tbA);
-    bulk_g2s(sm + kS2_GK, rec + kOffGK, 768, tbA);
-    pend_a = ci;
-  };
-  auto copy_u = [&](int ci) {
-    mbar_arrive_expect_tx(tbU, 32768);
-    bulk_g2s(sm + kS2_U, rec_of(ci) + kOffU, 32768, tbU);
-    pend_u = ci;
-  };
-  auto copy_b = [&](int ci) {
-    mbar_arrive_expect_tx(tbB, 8192);
-    bulk_g2s(sm + kS2_P, rec_of(ci) + kOffP, 8192, tbB);
-    pend_b = ci;
-  };
-  // Raw Q (or K) rows of chunk ci into their tile: one committed group per call
-  // (empty past the last chunk, so group counting stays uniform).
-  auto load_rows = [&](int ci, const __nv_bfloat16* src, int tile) {
-    if (ci < nchunks) {
+
+  if (warp == 9) {
+    // ---------------- loads ----------------
+    // Outstanding bulk copies (lane 0's view), drained on exit.
+    int pend_w = -1, pend_u = -1, pend_p = -1;
+    auto rows = [&](int ci, const __nv_bfloat16* src, int tile, uint64_t* bar) {
       const int c0 = start + ci * kC;
       const int n = min(kC, end - c0);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int p = it * 8 + warp;
+      // Lane l covers row (8 rg + l % 8) and chunk (4 kg + l / 8): eight
+      // consecutive rows per quarter warp keep the shared-memory writes
+      // conflict-free, four chunks per row keep global reads in 64-byte runs.
+#pragma unroll 4
+      for (int p = 0; p < 32; ++p) {
         const int r = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
         const bool valid = r < n;
         cp_async16(sm + tile + tile_off(r, kc * 8, 128),
                    src + (int64_t)(c0 + (valid ? r : 0)) * qk_stride + (int64_t)gh * kD + kc * 8,
                    valid ? 16u : 0u);
       }
-    }
-    cp_async_commit();
-  };
-  if (records_ok && nchunks > 0) {
-    if (tid == 0) {
-      copy_a(0);
-      copy_u(0);
-      copy_b(0);
-    }
-    load_rows(0, q, kS2_Q);
-    load_rows(0, k, kS2_K);
-  }
-
-  // Output write-back of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r, done by
-  // warps 4-7 only (warp 4 + q reads TMEM lanes 32q..32q+31, i.e. rows i, all
-  // 64 token columns), so warps 0-3 (warp 0 issues the MMAs) never wait for
-  // it. The values go through a [64 r][128 i] BF16 staging tile in the Delta^T
-  // area (unused at this point; the callers put a block-wide barrier before
-  // the area is written again) and leave as 16-byte vectors along dv.
-  auto write_outputs = [&](int cj) {
-    const int c0 = start + cj * kC;
-    const int n = min(kC, end - c0);
-    const float* qsb = qs + 64 * (cj & 1);
-    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + kS2_DA);
-    if (!mbar_wait(obar, cj & 1)) atomicExch(s_fail, 1);
-    fence_after_sync();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float o1[32], o2[32];
-      tmem_ld32(tmem_warp_addr(taddr, 256 + 64 * (cj & 1) + 32 * half), o1);
-      tmem_ld32(tmem_warp_addr(taddr, 384 + 64 * (cj & 1) + 32 * half), o2);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int r = 32 * half + e;
-        stage[r * kD + row] = __float2bfloat16_rn(fmaf(o1[e], qsb[r], o2[e]));
+      cp_async_commit();
+      cp_async_wait_group<0>();
+      fence_smem_to_async();
+      mbar_arrive(bar);
+    };
+    auto copy_w = [&](int ci) {
+      mbar_arrive_expect_tx(bW, 32768 + 768);
+      bulk_g2s(sm + kS2_W, rec_of(ci) + kOffW, 32768, bW);
+      bulk_g2s(sm + kS2_GK, rec_of(ci) + kOffGK, 768, bW);
+      pend_w = ci;
+    };
+    auto copy_u = [&](int ci) {
+      mbar_arrive_expect_tx(bU, 32768);
+      bulk_g2s(sm + kS2_U, rec_of(ci) + kOffU, 32768, bU);
+      pend_u = ci;
+    };
+    auto copy_p = [&](int ci) {
+      mbar_arrive_expect_tx(bP, 8192);
+      bulk_g2s(sm + kS2_P, rec_of(ci) + kOffP, 8192, bP);
+      pend_p = ci;
+    };
+    if (records_ok) {
+      if (lane == 0) {
+        copy_w(0);
+        copy_u(0);
+        copy_p(0);
+      }
+      rows(0, q, kS2_Q, bQ);
+      rows(0, k, kS2_K, bK);
+      for (int ci = 0; ci + 1 < nchunks; ++ci) {
+        const uint32_t par = ci & 1;
+        // Each buffer is refilled once the chunk's last reader of it is done;
+        // these events happen in this order.
+        if (wait(bX, par) && lane == 0) copy_w(ci + 1);
+        if (wait(bO1, par)) rows(ci + 1, q, kS2_Q, bQ);
+        if (wait(bDr, par) && lane == 0) copy_u(ci + 1);
+        if (wait(bS, par)) rows(ci + 1, k, kS2_K, bK);
+        if (wait(bO, par) && lane == 0) copy_p(ci + 1);
       }
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");   // warps 4-7 only
-    const int t = tid - 128;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int c = t + 128 * it;          // 16-byte chunk: token c / 16, dims 8 (c % 16)
-      const int r = c >> 4;
-      if (r < n)
-        *reinterpret_cast<uint4*>(o + ((int64_t)(c0 + r) * Hv + h) * kD + (c & 15) * 8) =
-            reinterpret_cast<const uint4*>(stage)[c];
+    if (lane == 0) {
+      // Bounded, not abortable: copies in flight must land before exit.
+      if (pend_w >= 0) mbar_wait(bW, pend_w & 1);
+      if (pend_u >= 0) mbar_wait(bU, pend_u & 1);
+      if (pend_p >= 0) mbar_wait(bP, pend_p & 1);
     }
-  };
-
-  const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
-  uint32_t phase = 0;
-  int done = 0;   // chunks whose MMAs completed (their outputs may still be pending)
-  for (int ci = 0; ci < nchunks && records_ok; ++ci) {
-    const int c0 = start + ci * kC;
-    const int n = min(kC, end - c0);
-    const uint32_t par = ci & 1;
-    const uint32_t o1col = 256 + 64 * par, o2col = 384 + 64 * par;
-    if (!mbar_wait(tbA, par)) atomicExch(s_fail, 1);
-    if (tid == 0) pend_a = -1;
-    const float glast = gk[n - 1];
-    const float gamma_c = exp2_nonpos(glast);
-    if (tid < 64) {
-      const bool in = tid < n;
-      dks[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
-      qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
+    __syncwarp();
+  } else if (warp == 8) {
+    // ---------------- MMAs (one lane) ----------------
+    if (lane == 0 && records_ok) {
+      const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
+      const uint32_t sah = smem_u32(sm + kS2_SAH), sal = smem_u32(sm + kS2_SAL);
+      const uint32_t w = smem_u32(sm + kS2_W), qt = smem_u32(sm + kS2_Q);
+      const uint32_t da = smem_u32(sm + kS2_DA), p = smem_u32(sm + kS2_P);
+      const uint32_t ddh = smem_u32(sm + kS2_DDH), ddl = smem_u32(sm + kS2_DDL);
+      const uint32_t kt = smem_u32(sm + kS2_K);
+      uint64_t* last = nullptr;
+      uint32_t last_par = 0;
+      for (int ci = 0; ci < nchunks; ++ci) {
+        const uint32_t par = ci & 1;
+        const uint32_t o1col = 256 + 64 * par, o2col = 384 + 64 * par;
+        // X^T = S W^T: cols [128, 192) S_hi W_hi^T + S_lo W_hi^T, cols
+        // [192, 256) S_hi W_lo^T (the record's W tile is [W hi; W lo], N = 128).
+        bool ok = wait(bW, par);
+        ok = wait(bSr, par) && ok;
+        fence_after_sync();
+        if (ok) {
+          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(w, 128, kk), id64 | kTransB, 1);
+          mma_commit(bX);
+        }
+        // O1^T = S Q^T (single BF16: the output is BF16).
+        if (wait(bQ, par) && ok) {
+          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
+          mma_commit(bO1);
+          last = bO1;
+          last_par = par;
+        }
+        // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
+        ok = wait(bDr, par);
+        ok = wait(bK, par) && ok;
+        ok = wait(bP, par) && ok;
+        fence_after_sync();
+        if (ok) {
+          const uint32_t idk = id128 | kTransB;
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), mn_desc(kt, 128, kk), idk, 1);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), mn_desc(kt, 128, kk), idk, 1);
+          mma_commit(bS);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + o2col, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, kk > 0);
+          mma_commit(bO);
+          last = bO;
+          last_par = par;
+        }
+      }
+      // Bounded, not abortable: the MMAs in flight must finish before exit.
+      if (last != nullptr) mbar_wait(last, last_par);
     }
-    // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
+    __syncwarp();
+  } else {
+    // ---------------- rows (warps 0-7) ----------------
+    const bool init = has_init != nullptr && has_init[seq] != 0;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-      const int cb = 64 * hf + 32 * blk;
-      float sv[32];
-      tmem_ld32(tmem_warp_addr(taddr, cb), sv);
+      const int c0 = 64 * hf + 32 * blk;
+      float vbuf[32];
 #pragma unroll
-      for (int e8 = 0; e8 < 4; ++e8) {
-        uint4 hi, lo;
-        split8(sv + 8 * e8, hi, lo);
-        *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb + 8 * e8, 128)) = hi;
-        *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb + 8 * e8, 128)) = lo;
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f4 = init ? *reinterpret_cast<const float4*>(Sg + c0 + e)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        vbuf[e] = f4.x; vbuf[e + 1] = f4.y; vbuf[e + 2] = f4.z; vbuf[e + 3] = f4.w;
       }
-#pragma unroll
-      for (int e = 0; e < 32; ++e) sv[e] *= gamma_c;
-      tmem_st32(tmem_warp_addr(taddr, cb), sv);
+      tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
     }
-    cp_async_wait_group<1>();   // this chunk's Q rows (its K rows may still be landing)
-    fence_smem_to_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    // (c) X^T = S W^T (hi/lo: three products in two MMA groups) -> cols
-    // [128, 256), summed by the Delta step;  O1^T = S Q^T -> o1col.
-    if (tid == 0) {
-      const uint32_t sah = smem_u32(sm + kS2_SAH), sal = smem_u32(sm + kS2_SAL);
-      const uint32_t w = smem_u32(sm + kS2_W);
-      const uint32_t qt = smem_u32(sm + kS2_Q);
-      // cols [128, 192): S_hi W_hi^T + S_lo W_hi^T;  cols [192, 256): S_hi W_lo^T
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(w, 128, kk), id64 | kTransB, 1);
-      mma_commit(mbar);   // X is what Delta waits for; O1 completes with the output barrier
-      for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
-      mma_commit(qbar);   // the Q tile may be refilled once O1 has read it
-      pend_q = ci;
-      // P is read by the previous chunk's O2 MMAs (the output barrier): this
-      // chunk's P replaces it only after they are done.
-      if (ci >= 1) {
-        if (!mbar_wait(obar, (ci - 1) & 1)) atomicExch(s_fail, 1);
-        pend_o = -1;
-        copy_b(ci);
-      }
-    }
-    // Warps 4-7 write the previous chunk's outputs while these MMAs run.
-    if (done > 0 && warp >= 4) write_outputs(ci - 1);
-    if (!mbar_wait(mbar, phase)) atomicExch(s_fail, 1);
-    phase ^= 1;
-    fence_after_sync();
-    // W and the gates are free: fetch the next chunk's.
-    if (tid == 0 && ci + 1 < nchunks) copy_a(ci + 1);
-    if (!mbar_wait(tbU, par)) atomicExch(s_fail, 1);
-    if (tid == 0) pend_u = -1;
-    fence_before_sync();
-    __syncthreads();   // the output staging in the Delta^T area has been read
-    // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
-    {
-      float xv[32], xl[32];
-      tmem_ld32(tmem_warp_addr(taddr, 128 + 32 * hf), xv);
-      tmem_ld32(tmem_warp_addr(taddr, 192 + 32 * hf), xl);
+    auto row_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r through a
+    // [64 r][128 i] BF16 staging tile in the Delta^T area (its readers, the
+    // chunk's MMAs, are done), leaving as 16-byte vectors along dv.
+    auto write_outputs = [&](int cj) {
+      const int c0 = start + cj * kC;
+      const int n = min(kC, end - c0);
+      const float* qsb = qs + 64 * (cj & 1);
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + kS2_DA);
+      wait(bO, cj & 1);
+      __syncwarp();
+      fence_after_sync();
+      {
+        float o1[32], o2[32];
+        tmem_ld32x2(tmem_warp_addr(taddr, 256 + 64 * (cj & 1) + 32 * hf),
+                    tmem_warp_addr(taddr, 384 + 64 * (cj & 1) + 32 * hf), o1, o2);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) xv[e] += xl[e];
-#pragma unroll
-      for (int e8 = 0; e8 < 4; ++e8) {
-        const float4 u0 = us[row * 16 + ((8 * hf + 2 * e8) ^ (row & 7))];
-        const float4 u1 = us[row * 16 + ((8 * hf + 2 * e8 + 1) ^ (row & 7))];
-        const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        float dl[8], dd[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = 32 * hf + 8 * e8 + e;
-          const float del = r < n ? uu[e] - xv[8 * e8 + e] : 0.f;
-          dl[e] = del;
-          dd[e] = del * dks[r];
+        for (int e = 0; e < 32; ++e) {
+          const int r = 32 * hf + e;
+          stage[r * kD + row] = __float2bfloat16_rn(fmaf(o1[e], qsb[r], o2[e]));
         }
-        const int s0 = 32 * hf + 8 * e8;
-        uint4 hi, lo;
-        *reinterpret_cast<uint4*>(sm + kS2_DA + tile_off(row, s0, 64)) = pack8(dl);
-        split8(dd, hi, lo);
-        *reinterpret_cast<uint4*>(sm + kS2_DDH + tile_off(row, s0, 64)) = hi;
-        *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(row, s0, 64)) = lo;
+      }
+      row_sync();
+      if (!failed()) {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int c = tid + kRowThreads * it;   // 16-byte chunk: token c / 16, dims 8 (c % 16)
+          const int r = c >> 4;
+          if (r < n)
+            *reinterpret_cast<uint4*>(o + ((int64_t)(c0 + r) * Hv + h) * kD + (c & 15) * 8) =
+                reinterpret_cast<const uint4*>(stage)[c];
+        }
+      }
+      row_sync();   // the staging tile is read before Delta overwrites it
+    };
+
+    for (int ci = 0; ci < nchunks && records_ok; ++ci) {
+      const int c0 = start + ci * kC;
+      const int n = min(kC, end - c0);
+      const uint32_t par = ci & 1;
+      // The chunk's gates (the loader refills them only after this chunk's
+      // X MMAs, which wait for the S tiles below).
+      wait(bW, par);
+      const float glast = gk[n - 1];
+      const float gamma_c = exp2_nonpos(glast);
+      float* dkb = dks + 64 * par;
+      if (tid < 64) {
+        const bool in = tid < n;
+        dkb[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
+        qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
+      }
+      // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
+      if (ci > 0) wait(bS, (ci - 1) & 1);
+      __syncwarp();
+      fence_after_sync();
+      {
+        const int cb0 = 64 * hf, cb1 = 64 * hf + 32;
+        float s0[32], s1[32];
+        tmem_ld32x2(tmem_warp_addr(taddr, cb0), tmem_warp_addr(taddr, cb1), s0, s1);
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          uint4 hi, lo;
+          split8(s0 + 8 * e8, hi, lo);
+          *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb0 + 8 * e8, 128)) = hi;
+          *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb0 + 8 * e8, 128)) = lo;
+          split8(s1 + 8 * e8, hi, lo);
+          *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb1 + 8 * e8, 128)) = hi;
+          *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb1 + 8 * e8, 128)) = lo;
+        }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          s0[e] *= gamma_c;
+          s1[e] *= gamma_c;
+        }
+        tmem_st32x2(tmem_warp_addr(taddr, cb0), tmem_warp_addr(taddr, cb1), s0, s1);
+      }
+      fence_smem_to_async();
+      fence_before_sync();
+      mbar_arrive(bSr);
+      // The previous chunk's outputs while this chunk's X MMAs run.
+      if (ci > 0) write_outputs(ci - 1);
+      else row_sync();   // dks and qs are written before Delta reads them
+      // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
+      wait(bX, par);
+      __syncwarp();
+      fence_after_sync();
+      {
+        float xv[32], xl[32];
+        tmem_ld32x2(tmem_warp_addr(taddr, 128 + 32 * hf), tmem_warp_addr(taddr, 192 + 32 * hf),
+                    xv, xl);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xv[e] += xl[e];
+        wait(bU, par);
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          const float4 u0 = us[row * 16 + ((8 * hf + 2 * e8) ^ (row & 7))];
+          const float4 u1 = us[row * 16 + ((8 * hf + 2 * e8 + 1) ^ (row & 7))];
+          const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          float dl[8], dd[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int r = 32 * hf + 8 * e8 + e;
+            const float del = r < n ? uu[e] - xv[8 * e8 + e] : 0.f;
+            dl[e] = del;
+            dd[e] = del * dkb[r];
+          }
+          const int s0 = 32 * hf + 8 * e8;
+          uint4 hi, lo;
+          *reinterpret_cast<uint4*>(sm + kS2_DA + tile_off(row, s0, 64)) = pack8(dl);
+          split8(dd, hi, lo);
+          *reinterpret_cast<uint4*>(sm + kS2_DDH + tile_off(row, s0, 64)) = hi;
+          *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(row, s0, 64)) = lo;
+        }
+      }
+      fence_smem_to_async();
+      fence_before_sync();
+      mbar_arrive(bDr);
+    }
+    if (records_ok && nchunks > 0) {
+      write_outputs(nchunks - 1);
+      wait(bS, (nchunks - 1) & 1);
+      __syncwarp();
+      fence_after_sync();
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const int cb = 64 * hf + 32 * blk;
+        float sv[32];
+        tmem_ld32(tmem_warp_addr(taddr, cb), sv);
+        if (!failed()) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(Sg + cb + e) =
+                make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
+        }
       }
     }
-    cp_async_wait_group<0>();   // this chunk's K rows
-    // The Q tile is read by this chunk's O1 MMAs, which the first barrier does
-    // not cover (long done by now): then the next chunk's Q rows replace it.
-    if (!mbar_wait(qbar, par)) atomicExch(s_fail, 1);
-    if (tid == 0) pend_q = -1;
-    load_rows(ci + 1, q, kS2_Q);
-    fence_smem_to_async();
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    // (e) O2^T = Delta^T P^T;  S += (Delta^T D) K  (hi and lo passes).
-    if (tid == 0) {
-      if (ci + 1 < nchunks) copy_u(ci + 1);     // every thread is done with this U
-      if (!mbar_wait(tbB, par)) atomicExch(s_fail, 1);
-      pend_b = -1;
-      if (!*s_fail) {
-        const uint32_t da = smem_u32(sm + kS2_DA), p = smem_u32(sm + kS2_P);
-        const uint32_t ddh = smem_u32(sm + kS2_DDH), ddl = smem_u32(sm + kS2_DDL);
-        const uint32_t kt = smem_u32(sm + kS2_K);
-        const uint32_t idk = id128 | kTransB;
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), mn_desc(kt, 128, kk), idk, 1);
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), mn_desc(kt, 128, kk), idk, 1);
-        mma_commit(mbar);   // the next chunk needs only S
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + o2col, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, kk > 0);
-        mma_commit(obar);
-        pend_o = ci;
-      }
-    }
-    __syncthreads();
-    if (*s_fail) break;
-    if (!mbar_wait(mbar, phase)) atomicExch(s_fail, 1);
-    phase ^= 1;
-    fence_after_sync();
-    done = ci + 1;
-    // The K tile is free (P is refilled after this chunk's O2, in the next
-    // chunk): fetch the next chunk's K rows.
-    load_rows(ci + 1, k, kS2_K);
-    fence_before_sync();
-    __syncthreads();
-    if (*s_fail) break;
+    if (tid == 0 && (failed() || !records_ok))
+      atomicExch(hdr + 2, (int)(failed() ? GDN_ERR_TIMEOUT : GDN_ERR_INVALID_ARG));
+    __syncwarp();
   }
   cp_async_wait_all();
-  if (!*s_fail && records_ok) {
-    if (done > 0 && warp >= 4) write_outputs(done - 1);
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {
-      const int cb = 64 * hf + 32 * blk;
-      float sv[32];
-      tmem_ld32(tmem_warp_addr(taddr, cb), sv);
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(Sg + cb + e) = make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
-    }
-  } else if (tid == 0) {
-    atomicExch(hdr + 2, (int)(*s_fail ? GDN_ERR_TIMEOUT : GDN_ERR_INVALID_ARG));
-  }
-  // After an early exit, record copies may still be landing: wait (bounded)
-  // for them before the CTA's shared memory is released.
-  if (tid == 0) {
-    if (pend_a >= 0) mbar_wait(tbA, pend_a & 1);
-    if (pend_u >= 0) mbar_wait(tbU, pend_u & 1);
-    if (pend_b >= 0) mbar_wait(tbB, pend_b & 1);
-    if (pend_q >= 0) mbar_wait(qbar, pend_q & 1);
-    if (pend_o >= 0) mbar_wait(obar, pend_o & 1);
-  }
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(taddr, 512);

@@ -143,6 +143,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity,
   return true;
 }
 
+// One plain arrival (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(mbar)) : "memory");
+}
+
 // ---- bulk (TMA, 1-D) and 16-byte asynchronous copies ----------------------
 // Arm the mbarrier for `bytes` of incoming bulk copies (plus one arrival).
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
@@ -253,6 +258,39 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
          "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
          "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
          "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// Two 32-column loads (possibly of different TMEM regions) and one wait, so
+// that the second load's latency overlaps the first's.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32],
+                                            float (&vb)[32]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(ta), "r"(tb) : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// Two 32-column stores and one wait.
+__device__ __forceinline__ void tmem_st32x2(uint32_t ta, uint32_t tb, const float (&va)[32],
+                                            const float (&vb)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%1], "
+      "{%34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(ta), "r"(tb), "r"(__float_as_uint(va[0])), "r"(__float_as_uint(va[1])), "r"(__float_as_uint(va[2])), "r"(__float_as_uint(va[3])), "r"(__float_as_uint(va[4])), "r"(__float_as_uint(va[5])), "r"(__float_as_uint(va[6])), "r"(__float_as_uint(va[7])), "r"(__float_as_uint(va[8])), "r"(__float_as_uint(va[9])), "r"(__float_as_uint(va[10])), "r"(__float_as_uint(va[11])), "r"(__float_as_uint(va[12])), "r"(__float_as_uint(va[13])), "r"(__float_as_uint(va[14])), "r"(__float_as_uint(va[15])), "r"(__float_as_uint(va[16])), "r"(__float_as_uint(va[17])), "r"(__float_as_uint(va[18])), "r"(__float_as_uint(va[19])), "r"(__float_as_uint(va[20])), "r"(__float_as_uint(va[21])), "r"(__float_as_uint(va[22])), "r"(__float_as_uint(va[23])), "r"(__float_as_uint(va[24])), "r"(__float_as_uint(va[25])), "r"(__float_as_uint(va[26])), "r"(__float_as_uint(va[27])), "r"(__float_as_uint(va[28])), "r"(__float_as_uint(va[29])), "r"(__float_as_uint(va[30])), "r"(__float_as_uint(va[31])), "r"(__float_as_uint(vb[0])), "r"(__float_as_uint(vb[1])), "r"(__float_as_uint(vb[2])), "r"(__float_as_uint(vb[3])), "r"(__float_as_uint(vb[4])), "r"(__float_as_uint(vb[5])), "r"(__float_as_uint(vb[6])), "r"(__float_as_uint(vb[7])), "r"(__float_as_uint(vb[8])), "r"(__float_as_uint(vb[9])), "r"(__float_as_uint(vb[10])), "r"(__float_as_uint(vb[11])), "r"(__float_as_uint(vb[12])), "r"(__float_as_uint(vb[13])), "r"(__float_as_uint(vb[14])), "r"(__float_as_uint(vb[15])), "r"(__float_as_uint(vb[16])), "r"(__float_as_uint(vb[17])), "r"(__float_as_uint(vb[18])), "r"(__float_as_uint(vb[19])), "r"(__float_as_uint(vb[20])), "r"(__float_as_uint(vb[21])), "r"(__float_as_uint(vb[22])), "r"(__float_as_uint(vb[23])), "r"(__float_as_uint(vb[24])), "r"(__float_as_uint(vb[25])), "r"(__float_as_uint(vb[26])), "r"(__float_as_uint(vb[27])), "r"(__float_as_uint(vb[28])), "r"(__float_as_uint(vb[29])), "r"(__float_as_uint(vb[30])), "r"(__float_as_uint(vb[31]))
       : "memory");
 }
 
