@@ -448,13 +448,14 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 //   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1^T = S Q^T once
 //     the S tiles are ready; S += (Delta^T D) K (hi/lo) and O2^T = Delta^T P^T
 //     once Delta is.
-//   warp 9: the next chunk's record (W and gates, U, P: bulk copies) and raw Q
-//     and K rows (16-byte asynchronous copies by all lanes), each as soon as
-//     the buffer it refills is free.
+//   warp 9: the next chunk's record (W and gates, U, P) by bulk copies, each
+//     as soon as the buffer it refills is free.
+//   warps 10 and 11: the next chunk's raw Q and K rows (16-byte asynchronous
+//     copies by all lanes) once the previous tile's readers are done.
 // TMEM: S [0, 128), X^T [128, 256) (two partial sums), O1^T and O2^T
 // double-buffered in [256, 384) and [384, 512).
 // ---------------------------------------------------------------------------
-constexpr int kThreads2 = 320;
+constexpr int kThreads2 = 384;
 constexpr int kRowThreads = 256;
 constexpr int kS2_SAH = 0;          // S hi  [128 i][128 j]                   32768
 constexpr int kS2_SAL = 32768;      // S lo                                   32768
@@ -560,29 +561,43 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     return records + ((size_t)(first + ci) * Hv + h) * kRecBytes;
   };
 
-  if (warp == 9) {
-    // ---------------- loads ----------------
+  // 16-byte asynchronous copies of chunk ci's raw rows (Q or K) into a tile by
+  // one warp, then one arrival per lane on `bar` once they have landed.
+  auto rows = [&](int ci, const __nv_bfloat16* src, int tile, uint64_t* bar) {
+    const int c0 = start + ci * kC;
+    const int n = min(kC, end - c0);
+    // Lane l covers row (8 rg + l % 8) and chunk (4 kg + l / 8): eight
+    // consecutive rows per quarter warp keep the shared-memory writes
+    // conflict-free, four chunks per row keep global reads in 64-byte runs.
+#pragma unroll 4
+    for (int p = 0; p < 32; ++p) {
+      const int r = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
+      const bool valid = r < n;
+      cp_async16(sm + tile + tile_off(r, kc * 8, 128),
+                 src + (int64_t)(c0 + (valid ? r : 0)) * qk_stride + (int64_t)gh * kD + kc * 8,
+                 valid ? 16u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait_group<0>();
+    fence_smem_to_async();
+    mbar_arrive(bar);
+  };
+  if (warp == 10 || warp == 11) {
+    // ---------------- Q rows (warp 10) or K rows (warp 11) ----------------
+    const bool is_q = warp == 10;
+    if (records_ok) {
+      rows(0, is_q ? q : k, is_q ? kS2_Q : kS2_K, is_q ? bQ : bK);
+      for (int ci = 0; ci + 1 < nchunks; ++ci) {
+        // Q is free once the chunk's O1 has read it, K once its S update has.
+        if (wait(is_q ? bO1 : bS, ci & 1))
+          rows(ci + 1, is_q ? q : k, is_q ? kS2_Q : kS2_K, is_q ? bQ : bK);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------- record copies and output stores ----------------
     // Outstanding bulk copies (lane 0's view), drained on exit.
     int pend_w = -1, pend_u = -1, pend_p = -1;
-    auto rows = [&](int ci, const __nv_bfloat16* src, int tile, uint64_t* bar) {
-      const int c0 = start + ci * kC;
-      const int n = min(kC, end - c0);
-      // Lane l covers row (8 rg + l % 8) and chunk (4 kg + l / 8): eight
-      // consecutive rows per quarter warp keep the shared-memory writes
-      // conflict-free, four chunks per row keep global reads in 64-byte runs.
-#pragma unroll 4
-      for (int p = 0; p < 32; ++p) {
-        const int r = (p >> 2) * 8 + (lane & 7), kc = (p & 3) * 4 + (lane >> 3);
-        const bool valid = r < n;
-        cp_async16(sm + tile + tile_off(r, kc * 8, 128),
-                   src + (int64_t)(c0 + (valid ? r : 0)) * qk_stride + (int64_t)gh * kD + kc * 8,
-                   valid ? 16u : 0u);
-      }
-      cp_async_commit();
-      cp_async_wait_group<0>();
-      fence_smem_to_async();
-      mbar_arrive(bar);
-    };
     auto copy_w = [&](int ci) {
       mbar_arrive_expect_tx(bW, 32768 + 768);
       bulk_g2s(sm + kS2_W, rec_of(ci) + kOffW, 32768, bW);
@@ -605,16 +620,12 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         copy_u(0);
         copy_p(0);
       }
-      rows(0, q, kS2_Q, bQ);
-      rows(0, k, kS2_K, bK);
       for (int ci = 0; ci + 1 < nchunks; ++ci) {
         const uint32_t par = ci & 1;
-        // Each buffer is refilled once the chunk's last reader of it is done;
-        // these events happen in this order.
+        // Each buffer is refilled once the chunk's last reader of it is
+        // done; these events happen in this order.
         if (wait(bX, par) && lane == 0) copy_w(ci + 1);
-        if (wait(bO1, par)) rows(ci + 1, q, kS2_Q, bQ);
         if (wait(bDr, par) && lane == 0) copy_u(ci + 1);
-        if (wait(bS, par)) rows(ci + 1, k, kS2_K, bK);
         if (wait(bO, par) && lane == 0) copy_p(ci + 1);
       }
     }
@@ -731,8 +742,12 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       const int c0 = start + ci * kC;
       const int n = min(kC, end - c0);
       const uint32_t par = ci & 1;
-      // The chunk's gates (the loader refills them only after this chunk's
-      // X MMAs, which wait for the S tiles below).
+      // Once the previous chunk's S update is done, so are every row
+      // thread's reads of the gate buffers this chunk refills (Delta two
+      // chunks ago, the outputs staged in the previous chunk). The record's
+      // gates are refilled only after this chunk's X MMAs, which wait for the
+      // S tiles below.
+      if (ci > 0) wait(bS, (ci - 1) & 1);
       wait(bW, par);
       const float glast = gk[n - 1];
       const float gamma_c = exp2_nonpos(glast);
@@ -743,7 +758,6 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
       }
       // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
-      if (ci > 0) wait(bS, (ci - 1) & 1);
       __syncwarp();
       fence_after_sync();
       {
