@@ -391,29 +391,36 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
     // consumed K/Q rows, U over V and the A area, gates over the scratch), then
     // write it with three bulk stores.
     // Lane j holds W[r][j] for all r: MN-major B tiles (N = r, K = j).
-    float w[32];
+    {
+      float w0[32], w1[32];
+      tmem_ld32x2(tmem_warp_addr(taddr, 0), tmem_warp_addr(taddr, 32), w0, w1);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tmem_warp_addr(taddr, 32 * half), w);
+      for (int half = 0; half < 2; ++half) {
+        const float* w = half ? w1 : w0;
 #pragma unroll
-      for (int rg = 0; rg < 4; ++rg) {
-        uint4 hi, lo;
-        split8(w + 8 * rg, hi, lo);
-        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(32 * half + 8 * rg, tid, 128)) = hi;
-        *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(64 + 32 * half + 8 * rg, tid, 128)) =
-            lo;
+        for (int rg = 0; rg < 4; ++rg) {
+          uint4 hi, lo;
+          split8(w + 8 * rg, hi, lo);
+          *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(32 * half + 8 * rg, tid, 128)) = hi;
+          *reinterpret_cast<uint4*>(sm + kS1_A1 + kOffW + mn_off(64 + 32 * half + 8 * rg, tid, 128)) =
+              lo;
+        }
       }
     }
     // Lane i holds U[r][i] for all r: row i (float32), its 16-byte chunk c at
     // position c ^ (i % 8) so that the state kernel reads one chunk per row
     // across a warp without bank conflicts.
-    float4* urow = reinterpret_cast<float4*>(sm + kS1_V) + tid * 16;
+    {
+      float4* urow = reinterpret_cast<float4*>(sm + kS1_V) + tid * 16;
+      float u0[32], u1[32];
+      tmem_ld32x2(tmem_warp_addr(taddr, 64), tmem_warp_addr(taddr, 96), u0, u1);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld32(tmem_warp_addr(taddr, 64 + 32 * half), w);
+      for (int half = 0; half < 2; ++half) {
+        const float* w = half ? u1 : u0;
 #pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        urow[(8 * half + e / 4) ^ (tid & 7)] = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+        for (int e = 0; e < 32; e += 4)
+          urow[(8 * half + e / 4) ^ (tid & 7)] = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+      }
     }
     if (tid < 64) {
       float* gk = reinterpret_cast<float*>(sm + kS1_RS);
@@ -495,9 +502,10 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   uint64_t* bO1 = bars + 8;   // O1 MMAs done              (commit)
   uint64_t* bS = bars + 9;    // S update done             (commit)
   uint64_t* bO = bars + 10;   // O2 MMAs (and all before) done (commit)
-  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 96);
-  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 100);
-  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 104);
+  uint64_t* bOr = bars + 11;  // outputs read from TMEM    (256 row threads)
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kS2_BAR + 104);
+  int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 108);
+  int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 112);
 
   const int seq = blockIdx.x, h = blockIdx.y, gh = h / (Hv / Hk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -514,9 +522,9 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   if (tid == 0) {
     *s_first = 0;
     *s_fail = 0;
-    for (int i = 0; i < 11; ++i) {
+    for (int i = 0; i < 12; ++i) {
       const bool rows_in = bars + i == bQ || bars + i == bK;
-      const bool rows_out = bars + i == bSr || bars + i == bDr;
+      const bool rows_out = bars + i == bSr || bars + i == bDr || bars + i == bOr;
       mbar_init(bars + i, rows_in ? 32u : (rows_out ? (uint32_t)kRowThreads : 1u));
     }
   }
@@ -649,7 +657,6 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       uint32_t last_par = 0;
       for (int ci = 0; ci < nchunks; ++ci) {
         const uint32_t par = ci & 1;
-        const uint32_t o1col = 256 + 64 * par, o2col = 384 + 64 * par;
         // X^T = S W^T: cols [128, 192) S_hi W_hi^T + S_lo W_hi^T, cols
         // [192, 256) S_hi W_lo^T (the record's W tile is [W hi; W lo], N = 128).
         bool ok = wait(bW, par);
@@ -660,14 +667,21 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(w, 128, kk), id64 | kTransB, 1);
           mma_commit(bX);
         }
-        // O1^T = S Q^T (single BF16: the output is BF16).
-        if (wait(bQ, par) && ok) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + o1col, tile_desc(sah, 128, kk), tile_desc(qt, 128, kk), id64, kk > 0);
+        // O1 = Q S^T into [token lane][dv column] (single BF16: the output is
+        // BF16). M = 128: rows 64-127 of the A operand are the K tile that
+        // follows Q in shared memory, results unused. The row warps must have
+        // read the previous chunk's outputs.
+        ok = wait(bQ, par) && ok;
+        if (ci > 0) ok = wait(bOr, (ci - 1) & 1) && ok;
+        fence_after_sync();
+        if (ok) {
+          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 256, tile_desc(qt, 128, kk), tile_desc(sah, 128, kk), id128, kk > 0);
           mma_commit(bO1);
           last = bO1;
           last_par = par;
         }
-        // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
+        // S += (Delta^T D) K (hi and lo passes);  O2 = P Delta (rows 64-127
+        // of the A operand: the 8 KB after P, results unused).
         ok = wait(bDr, par);
         ok = wait(bK, par) && ok;
         ok = wait(bP, par) && ok;
@@ -677,7 +691,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), mn_desc(kt, 128, kk), idk, 1);
           for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), mn_desc(kt, 128, kk), idk, 1);
           mma_commit(bS);
-          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + o2col, tile_desc(da, 64, kk), tile_desc(p, 64, kk), id64, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 384, tile_desc(p, 64, kk), tile_desc(da, 64, kk), id128, kk > 0);
           mma_commit(bO);
           last = bO;
           last_par = par;
@@ -703,39 +717,39 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
     }
     auto row_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r through a
-    // [64 r][128 i] BF16 staging tile in the Delta^T area (its readers, the
-    // chunk's MMAs, are done), leaving as 16-byte vectors along dv.
+    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r. O1 and O2 hold
+    // token r in TMEM lane r (lanes 0-63) and dv along the columns, so the
+    // threads of warps 0, 1, 4 and 5 each write 64 consecutive values of one
+    // output row as 16-byte vectors; every row thread then signals that the
+    // accumulators may be overwritten.
     auto write_outputs = [&](int cj) {
       const int c0 = start + cj * kC;
       const int n = min(kC, end - c0);
-      const float* qsb = qs + 64 * (cj & 1);
-      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + kS2_DA);
       wait(bO, cj & 1);
       __syncwarp();
       fence_after_sync();
-      {
-        float o1[32], o2[32];
-        tmem_ld32x2(tmem_warp_addr(taddr, 256 + 64 * (cj & 1) + 32 * hf),
-                    tmem_warp_addr(taddr, 384 + 64 * (cj & 1) + 32 * hf), o1, o2);
+      if ((warp & 3) < 2) {
+        const float qr = qs[64 * (cj & 1) + row];
+        __nv_bfloat16* dst = o + ((int64_t)(c0 + row) * Hv + h) * kD + 64 * hf;
+        const bool st = row < n && !failed();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int r = 32 * hf + e;
-          stage[r * kD + row] = __float2bfloat16_rn(fmaf(o1[e], qsb[r], o2[e]));
+        for (int half = 0; half < 2; ++half) {
+          float o1[32], o2[32];
+          tmem_ld32x2(tmem_warp_addr(taddr, 256 + 64 * hf + 32 * half),
+                      tmem_warp_addr(taddr, 384 + 64 * hf + 32 * half), o1, o2);
+          if (st) {
+#pragma unroll
+            for (int e8 = 0; e8 < 4; ++e8) {
+              float v8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v8[e] = fmaf(o1[8 * e8 + e], qr, o2[8 * e8 + e]);
+              *reinterpret_cast<uint4*>(dst + 32 * half + 8 * e8) = pack8(v8);
+            }
+          }
         }
       }
-      row_sync();
-      if (!failed()) {
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int c = tid + kRowThreads * it;   // 16-byte chunk: token c / 16, dims 8 (c % 16)
-          const int r = c >> 4;
-          if (r < n)
-            *reinterpret_cast<uint4*>(o + ((int64_t)(c0 + r) * Hv + h) * kD + (c & 15) * 8) =
-                reinterpret_cast<const uint4*>(stage)[c];
-        }
-      }
-      row_sync();   // the staging tile is read before Delta overwrites it
+      fence_before_sync();
+      mbar_arrive(bOr);
     };
 
     for (int ci = 0; ci < nchunks && records_ok; ++ci) {
@@ -784,9 +798,9 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       fence_smem_to_async();
       fence_before_sync();
       mbar_arrive(bSr);
+      row_sync();   // dks and qs are written before they are read
       // The previous chunk's outputs while this chunk's X MMAs run.
       if (ci > 0) write_outputs(ci - 1);
-      else row_sync();   // dks and qs are written before Delta reads them
       // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
       wait(bX, par);
       __syncwarp();
