@@ -555,10 +555,22 @@ conv_update_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                    const __nv_bfloat16* __restrict__ w, const __nv_bfloat16* __restrict__ bias,
                    __nv_bfloat16* __restrict__ state, int C, int silu,
                    __nv_bfloat16* __restrict__ y, const StateSlots slots) {
-  pdl_wait();
-  pdl_trigger();
   const int n = blockIdx.y;
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * 8;
+  if (c0 < C) {
+    // Warm L2 with this thread's taps, bias and state while the previous
+    // kernel finishes.
+    const int s0 = state_slot(slots, n);
+    prefetch_l2(w + (size_t)c0 * 4);
+    if (bias) prefetch_l2(bias + c0);
+    if (s0 >= 0) {
+      const __nv_bfloat16* sp = state + ((size_t)s0 * C + c0) * 3;
+      prefetch_l2(sp);
+      prefetch_l2(sp + 23);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
   const int slot = state_slot(slots, n);
   if (c0 >= C || slot < 0) return;
   float wf[4][8], bf[8], win[3][8], xc[8], out[8];

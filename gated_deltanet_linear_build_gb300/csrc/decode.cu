@@ -247,8 +247,6 @@ delta_decode_stream_kernel(const DecodeArgs p) {
     }
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
   auto unit_coords = [&](int unit, int& n, int& h, int& g, int& part) {
     const int nh = unit / kDecUnitsPerHead;
     part = unit - nh * kDecUnitsPerHead;
@@ -256,6 +254,20 @@ delta_decode_stream_kernel(const DecodeArgs p) {
     h = nh - n * Hv;
     g = h / ratio;
   };
+  if (!kFused && warp == Cfg::kProdWarp && lane == 0) {
+    // Warm L2 with the state rows of the first stages while the previous
+    // kernel finishes.
+    for (int i = 0; i < my_units && i < kDecStages; ++i) {
+      int n, h, g, part;
+      unit_coords(blockIdx.x + i * G, n, h, g, part);
+      const int slot = state_slot(p.slots, n);
+      if (slot >= 0)
+        bulk_prefetch_l2(p.S + (((size_t)slot * Hv + h) * kDecUnitsPerHead + part) * kDecRows * 128,
+                         kDecUnitBytes);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
 
   if constexpr (kFused) {
     if (warp == Cfg::kProdWarp + 1) {
