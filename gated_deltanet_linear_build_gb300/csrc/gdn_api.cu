@@ -5,6 +5,7 @@
 #include <string>
 
 #include "gdn_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -23,9 +24,31 @@ void set_cuda_error(cudaError_t e) {
 }
 }  // namespace gdn
 
+namespace gdn {
+namespace {
+// One CTA waits, with the library's bounded wait, for a phase of a freshly
+// initialised mbarrier that nothing completes.
+__global__ void bounded_wait_selftest_kernel(int32_t* status, long long max_cycles) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+  __syncthreads();
+  const bool completed = tc::mbar_wait(&bar, 0, max_cycles);
+  if (threadIdx.x == 0) *status = completed ? GDN_OK : GDN_ERR_TIMEOUT;
+}
+}  // namespace
+}  // namespace gdn
+
 using namespace gdn;
 
 extern "C" {
+
+gdn_status_t gdn_selftest_bounded_wait(int32_t* device_status, int64_t max_cycles,
+                                       void* stream) {
+  if (!device_status || max_cycles < 1 || max_cycles > 4000000000LL) return GDN_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      device_status, (long long)max_cycles);
+  return check_launch();
+}
 
 const char* gdn_status_string(gdn_status_t s) {
   switch (s) {

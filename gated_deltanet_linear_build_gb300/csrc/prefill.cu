@@ -178,7 +178,8 @@ state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
                   float* __restrict__ S, const uint8_t* __restrict__ has_init,
                   __nv_bfloat16* __restrict__ o, int Hk, int Hv, int qk_l2norm,
                   const float* __restrict__ g_ws, const float* __restrict__ w_ws,
-                  const float* __restrict__ u_ws, const StateSlots slots) {
+                  const float* __restrict__ u_ws, const int32_t* __restrict__ bstatus,
+                  const StateSlots slots) {
   constexpr int PK = DK + 1, PT = kChunk + 1, PS = SL + 1;
   extern __shared__ float smem[];
   float* Ss = smem;                  // [SL][PK]   state rows i (slice), columns j
@@ -197,6 +198,9 @@ state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   if (end <= start || start < 0 || end > T) return;
   const int slot = state_slot(slots, seq);
   if (slot < 0) return;   // a padding entry: state and outputs untouched
+  // Malformed cu_seqlens: the builder produced no chunks, so the per-token
+  // workspace rows were never written; leave state and outputs untouched.
+  if (*bstatus != GDN_OK) return;
   float* Sg = S + ((size_t)slot * Hv + h) * DV * DK + (size_t)i0 * DK;
   const bool init = has_init != nullptr && has_init[seq] != 0;
   for (int idx = tid; idx < SL * DK; idx += kThreads) {
@@ -311,7 +315,7 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   if ((rc = check_launch()) != GDN_OK) return rc;
   k2<<<dim3(N, Hv, DV / SL), kThreads, smem2, st>>>(qp, kp, qk_stride, cu, T, S, has_init,
                                                     static_cast<__nv_bfloat16*>(o), Hk, Hv, l2,
-                                                    g_ws, w_ws, u_ws, slots);
+                                                    g_ws, w_ws, u_ws, bstatus, slots);
   return check_launch();
 }
 

@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "gdn_causal_conv1d_update_slots",
     "gdn_delta_rule_decode_slots",
     "gdn_delta_rule_prefill_chunked_slots",
+    "gdn_selftest_bounded_wait",
     "gdn_status_string",
     "gdn_last_cuda_error_string",
 )
@@ -85,6 +86,7 @@ _SIGNATURES = {
                                                             _I32, _I32, _P, _P, _P, _I32, _I32,
                                                             _I32, _I32, _I32, _I32, _P,
                                                             ctypes.c_size_t, _P, _I32, _P]),
+    "gdn_selftest_bounded_wait": (ctypes.c_int, [_P, _I64, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_cuda_error_string": (ctypes.c_char_p, []),
 }
@@ -296,6 +298,21 @@ def delta_rule_prefill_chunked_slots(q, k, v, a, b, cu_seqlens, S, has_initial_s
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
         chunk, int(qk_l2norm), _ptr(workspace), nbytes, _ptr(state_indices), ns, _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked_slots")
+
+
+def selftest_bounded_wait(device_status, *, max_cycles: int = 2_000_000, stream=None):
+    """One CTA waits for an mbarrier phase that nothing completes, with the
+    library's bounded wait; device_status int32 [1] becomes GDN_ERR_TIMEOUT."""
+    rc = _lib().gdn_selftest_bounded_wait(_ptr(device_status), int(max_cycles), _stream(stream))
+    _check(rc, "gdn_selftest_bounded_wait")
+
+
+def prefill_workspace_status(workspace):
+    """(descriptor builder status, state pass status) from a prefill workspace
+    once the call has completed (words 1 and 2; the second is defined for
+    dk = dv = 128 only)."""
+    w = workspace[:12].view(torch.int32).cpu()
+    return int(w[1]), int(w[2])
 
 
 def status_string(status: int) -> str:

@@ -245,7 +245,17 @@ GDN_API size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32
  *   workspace   device scratch of at least
  *               gdn_delta_rule_prefill_workspace_size(T, N, Hv, dk, dv, chunk)
  *               bytes, 256-byte aligned; contents on entry do not matter.
- *               The call owns it until the enqueued work completes.
+ *               The call owns it until the enqueued work completes. Once it
+ *               has, two int32 words report device-side failures, which the
+ *               host cannot see before launch: word 1 (byte offset 4) is the
+ *               chunk-descriptor builder's status (GDN_OK, or
+ *               GDN_ERR_INVALID_ARG for malformed cu_seqlens, which then count
+ *               as no chunks at all: state and outputs are left untouched);
+ *               for dk = dv = 128, word 2 (byte offset 8)
+ *               is the state pass's status (GDN_OK; GDN_ERR_INVALID_ARG when
+ *               the chunks do not cover a sequence, whose state and outputs
+ *               are then left untouched; GDN_ERR_TIMEOUT when a bounded
+ *               device-side wait gave up).
  */
 GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
                                             const void* v, int64_t v_stride,
@@ -347,6 +357,21 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_slots(
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
     int32_t chunk, int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
     const int32_t* state_indices, int32_t num_slots, void* stream);
+
+/*
+ * Self-test of the bounded device-side waits every kernel of this library
+ * uses on its mbarriers. Launches one CTA that waits, with that same wait, for
+ * an mbarrier phase that nothing completes, giving up after about
+ * `max_cycles` SM clock cycles (1 .. 4e9; the kernels use about 4e9, ~2 s).
+ * When the wait gives up, *device_status becomes GDN_ERR_TIMEOUT and the CTA
+ * exits normally: the context stays usable. GDN_OK would mean that the wait
+ * returned without its phase completing (a defect).
+ *
+ *   device_status  device int32 [1] (output).
+ * NULL device_status or max_cycles outside the range is GDN_ERR_INVALID_ARG.
+ */
+GDN_API gdn_status_t gdn_selftest_bounded_wait(int32_t* device_status, int64_t max_cycles,
+                                               void* stream);
 
 /* Static description of a status code (never NULL). */
 GDN_API const char* gdn_status_string(gdn_status_t status);

@@ -211,3 +211,10 @@ def test_state_slot_variants_validation(lib):
     bad = list(pre)
     bad[9] = 0
     assert p(*bad, A16, 8, None) == OK
+
+
+def test_selftest_bounded_wait_validation(lib):
+    f = lib.gdn_selftest_bounded_wait
+    assert f(None, 1000, None) == INVALID
+    assert f(A16, 0, None) == INVALID
+    assert f(A16, 5000000000, None) == INVALID
