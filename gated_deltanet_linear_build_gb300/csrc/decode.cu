@@ -150,11 +150,11 @@ constexpr int kDecUnitsPerHead = 128 / kDecRows;
 constexpr int kFxQ = 0, kFxK = kFxQ + 256, kFxV = kFxK + 256;
 constexpr int kFsQ = kFxV + 128, kFsK = kFsQ + 768, kFsV = kFsK + 768;
 constexpr int kFSlot = kFsV + 384;                 // 2560 bytes
-constexpr int kFSlots = 6;
+constexpr int kFSlots = 8;
 constexpr int kFConv = 320;                        // conv channels of a unit (q, k, v)
 constexpr int kFConvWarps = kFConv / 32;           // 10
 constexpr int kFYSlot = 640;                       // BF16 k | q | v of a unit (fused)
-constexpr int kFYSlots = 4;
+constexpr int kFYSlots = 8;
 template <bool kFused>
 struct DecStage {
   static constexpr int kConvOff = kDecStages * kDecStageBytes;            // fused: conv ring
@@ -237,7 +237,7 @@ delta_decode_stream_kernel(const DecodeArgs p) {
     }
     if constexpr (kFused) {
       for (int cs = 0; cs < kFSlots; ++cs) {
-        mbar_init(cfull + cs, 1);
+        mbar_init(cfull + cs, 32);   // one arrival per producer lane
         mbar_init(cempty + cs, kFConvWarps);
       }
       for (int ys = 0; ys < kFYSlots; ++ys) {
@@ -271,29 +271,39 @@ delta_decode_stream_kernel(const DecodeArgs p) {
 
   if constexpr (kFused) {
     if (warp == Cfg::kProdWarp + 1) {
-      // Conv-input producer (lane 0): x, state, taps and bias of the unit's
-      // q, k and v channels into the conv ring.
-      if (lane == 0) {
-        for (int i = 0; i < my_units; ++i) {
-          const int cs = i % kFSlots;
-          if (i >= kFSlots && !mbar_wait(cempty + cs, ((i / kFSlots) - 1) & 1)) break;
-          int n, h, g, part;
-          unit_coords(blockIdx.x + i * G, n, h, g, part);
-          unsigned char* dst = sm + Cfg::kConvOff + cs * kFSlot;
-          const int cq = g * 128, ck = p.Hk * 128 + g * 128;
-          const int cv = 2 * p.Hk * 128 + h * 128 + part * kDecRows;
-          const __nv_bfloat16* xr = p.x + n * p.x_stride;
-          const __nv_bfloat16* sr = p.st_in + (size_t)n * p.C * 3;
-          uint64_t* bar = cfull + cs;
-          mbar_arrive_expect_tx(bar, 640 + 1920);
-          bulk_g2s(dst + kFxQ, xr + cq, 256, bar);
-          bulk_g2s(dst + kFxK, xr + ck, 256, bar);
-          bulk_g2s(dst + kFxV, xr + cv, 128, bar);
-          bulk_g2s(dst + kFsQ, sr + (size_t)cq * 3, 768, bar);
-          bulk_g2s(dst + kFsK, sr + (size_t)ck * 3, 768, bar);
-          bulk_g2s(dst + kFsV, sr + (size_t)cv * 3, 384, bar);
+      // Conv-input producer: x and state of the unit's q, k and v channels
+      // into the conv ring as 160 16-byte asynchronous copies, five per lane
+      // (the slot's regions are contiguous in this order, so chunk t lands at
+      // byte 16 t); each lane arrives on the slot's barrier once its own
+      // copies have landed. Small bulk copies would queue in the copy engine
+      // behind the state rows.
+      for (int i = 0; i < my_units; ++i) {
+        const int cs = i % kFSlots;
+        const bool ok = i < kFSlots || mbar_wait(cempty + cs, ((i / kFSlots) - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        int n, h, g, part;
+        unit_coords(blockIdx.x + i * G, n, h, g, part);
+        unsigned char* dst = sm + Cfg::kConvOff + cs * kFSlot;
+        const int cq = g * 128, ck = p.Hk * 128 + g * 128;
+        const int cv = 2 * p.Hk * 128 + h * 128 + part * kDecRows;
+        const __nv_bfloat16* xr = p.x + n * p.x_stride;
+        const __nv_bfloat16* sr = p.st_in + (size_t)n * p.C * 3;
+#pragma unroll
+        for (int m = 0; m < 5; ++m) {
+          const int t = lane + 32 * m;
+          const __nv_bfloat16* src =
+              t < 16 ? xr + cq + 8 * t
+            : t < 32 ? xr + ck + 8 * (t - 16)
+            : t < 40 ? xr + cv + 8 * (t - 32)
+            : t < 88 ? sr + (size_t)cq * 3 + 8 * (t - 40)
+            : t < 136 ? sr + (size_t)ck * 3 + 8 * (t - 88)
+                      : sr + (size_t)cv * 3 + 8 * (t - 136);
+          cp_async16(dst + 16 * t, src, 16u);
         }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];"
+                     :: "r"(smem_u32(cfull + cs)) : "memory");
       }
+      cp_async_wait_all();   // no copy in flight when the warp exits
       return;
     }
     if (warp >= Cfg::kConvWarp0 && warp < Cfg::kConvWarp0 + kFConvWarps) {
