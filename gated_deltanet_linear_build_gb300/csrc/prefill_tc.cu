@@ -16,9 +16,11 @@
 //   state kernel, one CTA per (sequence, v-head), S [dv=128 x dk=128] float32
 //   resident in TMEM, chunks in order:
 //     X^T  = S W^T                  (S and W split into BF16 hi + lo: 3 MMAs)
-//     O1^T = S Q^T                  (single BF16: the output is BF16)
+//     O1   = Q S^T                  (single BF16: the output is BF16)
 //     Delta^T = U^T - X^T           (CUDA cores, lane i holds row i)
-//     O2^T = Delta^T P^T            (single BF16); o_r = e^{g_r} O1_r + O2_r
+//     O2   = P Delta                (single BF16); o_r = e^{g_r} O1_r + O2_r,
+//            token r in TMEM lane r; staged in shared memory and written out
+//            as whole 256-byte output rows
 //     S    = e^{g_last} S + (Delta^T diag(e^{g_last-g}))  K   (Delta split: 2 MMAs,
 //            accumulated onto the rescaled S in TMEM)
 //
@@ -452,15 +454,16 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 //   warps 0-7 (rows): warp w owns TMEM lanes 32 (w % 4) .. + 31 (row i of S)
 //     and column half w / 4. Per chunk: S -> BF16 hi/lo A tiles and
 //     S <- e^{g_last} S; the previous chunk's outputs; Delta = U - X.
-//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1^T = S Q^T once
-//     the S tiles are ready; S += (Delta^T D) K (hi/lo) and O2^T = Delta^T P^T
+//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1 = Q S^T once
+//     the S tiles are ready; S += (Delta^T D) K (hi/lo) and O2 = P Delta
 //     once Delta is.
 //   warp 9: the next chunk's record (W and gates, U, P) by bulk copies, each
 //     as soon as the buffer it refills is free.
 //   warps 10 and 11: the next chunk's raw Q and K rows (16-byte asynchronous
 //     copies by all lanes) once the previous tile's readers are done.
-// TMEM: S [0, 128), X^T [128, 256) (two partial sums), O1^T and O2^T
-// double-buffered in [256, 384) and [384, 512).
+// TMEM: S [0, 128), X^T [128, 256) (two partial sums), O1 [256, 384) and
+// O2 [384, 512): output dv of token r in lane r, column 256 + dv (O1) and
+// 384 + dv (O2).
 // ---------------------------------------------------------------------------
 constexpr int kThreads2 = 384;
 constexpr int kRowThreads = 256;
@@ -717,39 +720,51 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
     }
     auto row_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r. O1 and O2 hold
-    // token r in TMEM lane r (lanes 0-63) and dv along the columns, so the
-    // threads of warps 0, 1, 4 and 5 each write 64 consecutive values of one
-    // output row as 16-byte vectors; every row thread then signals that the
-    // accumulators may be overwritten.
+    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r. The threads of
+    // warps 0, 1, 4 and 5 (lanes 0-63: token = row) read 64 consecutive
+    // outputs of their token (dv from 64 hf) and stage them in the Delta^T
+    // tile (free until this chunk's Delta: the previous chunk's O2 has read
+    // it), 256 bytes per token with its 16-byte chunks XOR-swizzled by the
+    // token; once every row thread has released the accumulators, all of them
+    // write the staged rows out as whole 256-byte rows of o (16 lanes per
+    // row), so that each warp store covers four full lines.
     auto write_outputs = [&](int cj) {
       const int c0 = start + cj * kC;
       const int n = min(kC, end - c0);
       wait(bO, cj & 1);
       __syncwarp();
       fence_after_sync();
+      unsigned char* stg = sm + kS2_DA;
       if ((warp & 3) < 2) {
         const float qr = qs[64 * (cj & 1) + row];
-        __nv_bfloat16* dst = o + ((int64_t)(c0 + row) * Hv + h) * kD + 64 * hf;
-        const bool st = row < n && !failed();
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float o1[32], o2[32];
           tmem_ld32x2(tmem_warp_addr(taddr, 256 + 64 * hf + 32 * half),
                       tmem_warp_addr(taddr, 384 + 64 * hf + 32 * half), o1, o2);
-          if (st) {
 #pragma unroll
-            for (int e8 = 0; e8 < 4; ++e8) {
-              float v8[8];
+          for (int e8 = 0; e8 < 4; ++e8) {
+            float v8[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) v8[e] = fmaf(o1[8 * e8 + e], qr, o2[8 * e8 + e]);
-              *reinterpret_cast<uint4*>(dst + 32 * half + 8 * e8) = pack8(v8);
-            }
+            for (int e = 0; e < 8; ++e) v8[e] = fmaf(o1[8 * e8 + e], qr, o2[8 * e8 + e]);
+            const int j = 8 * hf + 4 * half + e8;
+            *reinterpret_cast<uint4*>(stg + row * 256 + ((j ^ (row & 15)) << 4)) = pack8(v8);
           }
         }
       }
       fence_before_sync();
       mbar_arrive(bOr);
+      row_sync();
+      if (!failed()) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const int t = (p * kRowThreads + tid) >> 4, j = tid & 15;
+          if (t < n)
+            *reinterpret_cast<uint4*>(o + ((int64_t)(c0 + t) * Hv + h) * kD + 8 * j) =
+                *reinterpret_cast<const uint4*>(stg + t * 256 + ((j ^ (t & 15)) << 4));
+        }
+      }
+      row_sync();   // the staging is read before Delta overwrites it
     };
 
     for (int ci = 0; ci < nchunks && records_ok; ++ci) {
@@ -771,7 +786,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         dkb[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
         qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
       }
-      // (b) this thread's half of S row i -> hi/lo A tiles; S <- e^{g_last} S.
+      // (b) this thread's half of S row i -> hi/lo A tiles, then S <- e^{g_last} S.
       __syncwarp();
       fence_after_sync();
       {
@@ -788,6 +803,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb1 + 8 * e8, 128)) = hi;
           *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb1 + 8 * e8, 128)) = lo;
         }
+        fence_smem_to_async();
+        fence_before_sync();
+        mbar_arrive(bSr);
+        // S <- e^{g_last} S, off the X MMAs' path: only this chunk's S update
+        // (after Delta, whose barrier also orders this store) touches S next.
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           s0[e] *= gamma_c;
@@ -795,9 +815,6 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
         tmem_st32x2(tmem_warp_addr(taddr, cb0), tmem_warp_addr(taddr, cb1), s0, s1);
       }
-      fence_smem_to_async();
-      fence_before_sync();
-      mbar_arrive(bSr);
       row_sync();   // dks and qs are written before they are read
       // The previous chunk's outputs while this chunk's X MMAs run.
       if (ci > 0) write_outputs(ci - 1);
