@@ -14,13 +14,14 @@
 //   (float32) and the gates and norms.
 //
 //   state kernel, one CTA per (sequence, v-head), S [dv=128 x dk=128] float32
-//   resident in TMEM, chunks in order:
+//   resident in TMEM, and its BF16 hi + lo parts beside it in TMEM, where the
+//   tensor core reads them as the A operand; chunks in order:
 //     X^T  = S W^T                  (S and W split into BF16 hi + lo: 3 MMAs)
-//     O1   = Q S^T                  (single BF16: the output is BF16)
+//     O1^T = S Q^T                  (single BF16: the output is BF16)
 //     Delta^T = U^T - X^T           (CUDA cores, lane i holds row i)
-//     O2   = P Delta                (single BF16); o_r = e^{g_r} O1_r + O2_r,
-//            token r in TMEM lane r; staged in shared memory and written out
-//            as whole 256-byte output rows
+//     O2^T = Delta^T P^T            (single BF16); o_r = e^{g_r} O1_r + O2_r,
+//            transposed through shared memory and written out as whole
+//            256-byte output rows
 //     S    = e^{g_last} S + (Delta^T diag(e^{g_last-g}))  K   (Delta split: 2 MMAs,
 //            accumulated onto the rescaled S in TMEM)
 //
@@ -452,29 +453,27 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 // each other through mbarriers only, so that no role waits for another's
 // instruction stream:
 //   warps 0-7 (rows): warp w owns TMEM lanes 32 (w % 4) .. + 31 (row i of S)
-//     and column half w / 4. Per chunk: S -> BF16 hi/lo A tiles and
+//     and column half w / 4. Per chunk: S -> BF16 hi/lo parts (in TMEM) and
 //     S <- e^{g_last} S; the previous chunk's outputs; Delta = U - X.
-//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1 = Q S^T once
-//     the S tiles are ready; S += (Delta^T D) K (hi/lo) and O2 = P Delta
+//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1^T = S Q^T once
+//     the S parts are ready (A operands read from TMEM, so S costs no shared
+//     memory traffic); S += (Delta^T D) K (hi/lo) and O2^T = Delta^T P^T
 //     once Delta is.
 //   warp 9: the next chunk's record (W and gates, U, P) by bulk copies, each
 //     as soon as the buffer it refills is free.
 //   warps 10 and 11: the next chunk's raw Q and K rows (16-byte asynchronous
 //     copies by all lanes) once the previous tile's readers are done.
-// TMEM: S [0, 128), X^T [128, 256) (two partial sums), O1 [256, 384) and
-// O2 [384, 512): output dv of token r in lane r, column 256 + dv (O1) and
-// 384 + dv (O2).
+// TMEM: S [0, 128), S hi [128, 192) and S lo [192, 256) as BF16 pairs (dk j
+// in column j / 2), X^T [256, 384) (two partial sums; once read, the Delta
+// parts as BF16 pairs of tokens), O1^T [384, 448) and O2^T [448, 512) (dv i
+// in lane i, token r in column r).
 // ---------------------------------------------------------------------------
 constexpr int kThreads2 = 384;
 constexpr int kRowThreads = 256;
-constexpr int kS2_SAH = 0;          // S hi  [128 i][128 j]                   32768
-constexpr int kS2_SAL = 32768;      // S lo                                   32768
-constexpr int kS2_DA = 65536;       // Delta^T [128 i][64 s]; output staging  16384
-constexpr int kS2_DDH = 81920;      // (Delta^T D) hi                         16384
-constexpr int kS2_DDL = 98304;      // (Delta^T D) lo                         16384
-constexpr int kS2_Q = 114688;       // Q rows [64 r][128 j] K-major B         16384
-constexpr int kS2_K = 131072;       // K rows [64 s][128 j] (MN-major B)      16384
-constexpr int kS2_R = 147456;       // the chunk's record
+constexpr int kS2_STG = 0;          // output staging [64 r][128 dv] BF16     16384
+constexpr int kS2_Q = 16384;        // Q rows [64 r][128 j] K-major B         16384
+constexpr int kS2_K = 32768;        // K rows [64 s][128 j] (MN-major B)      16384
+constexpr int kS2_R = 49152;        // the chunk's record
 constexpr int kS2_W = kS2_R + kOffW, kS2_P = kS2_R + kOffP;
 constexpr int kS2_U = kS2_R + kOffU, kS2_GK = kS2_R + kOffGK;
 constexpr int kS2_QS = kS2_R + kRecBytes;         // e^{g_r} rq_r, two chunks [2][64]
@@ -499,7 +498,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   uint64_t* bP = bars + 2;    // P landed                  (bulk copy)
   uint64_t* bQ = bars + 3;    // Q rows landed             (32 loader lanes)
   uint64_t* bK = bars + 4;    // K rows landed             (32 loader lanes)
-  uint64_t* bSr = bars + 5;   // S tiles written, S rescaled (256 row threads)
+  uint64_t* bSr = bars + 5;   // S hi/lo parts written     (256 row threads)
   uint64_t* bDr = bars + 6;   // Delta tiles written       (256 row threads)
   uint64_t* bX = bars + 7;    // X MMAs done               (commit)
   uint64_t* bO1 = bars + 8;   // O1 MMAs done              (commit)
@@ -651,50 +650,50 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     // ---------------- MMAs (one lane) ----------------
     if (lane == 0 && records_ok) {
       const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
-      const uint32_t sah = smem_u32(sm + kS2_SAH), sal = smem_u32(sm + kS2_SAL);
+      const uint32_t sah = taddr + 128, sal = taddr + 192;   // S hi / lo in TMEM
       const uint32_t w = smem_u32(sm + kS2_W), qt = smem_u32(sm + kS2_Q);
-      const uint32_t da = smem_u32(sm + kS2_DA), p = smem_u32(sm + kS2_P);
-      const uint32_t ddh = smem_u32(sm + kS2_DDH), ddl = smem_u32(sm + kS2_DDL);
-      const uint32_t kt = smem_u32(sm + kS2_K);
+      const uint32_t p = smem_u32(sm + kS2_P), kt = smem_u32(sm + kS2_K);
+      // TMEM column of K step kk (16 tokens) of a Delta part based at `col`
+      auto dcol = [&](int col, int kk) { return taddr + col + 8 * kk + (kk >= 2 ? 16 : 0); };
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
       for (int ci = 0; ci < nchunks; ++ci) {
         const uint32_t par = ci & 1;
-        // X^T = S W^T: cols [128, 192) S_hi W_hi^T + S_lo W_hi^T, cols
-        // [192, 256) S_hi W_lo^T (the record's W tile is [W hi; W lo], N = 128).
+        // X^T = S W^T: cols [256, 320) S_hi W_hi^T + S_lo W_hi^T, cols
+        // [320, 384) S_hi W_lo^T (the record's W tile is [W hi; W lo], N = 128);
+        // one K = 16 step of a TMEM A operand is 8 columns.
         bool ok = wait(bW, par);
         ok = wait(bSr, par) && ok;
         fence_after_sync();
         if (ok) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sah, 128, kk), mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
-          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 128, tile_desc(sal, 128, kk), mn_desc(w, 128, kk), id64 | kTransB, 1);
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sah + 8 * kk, mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sal + 8 * kk, mn_desc(w, 128, kk), id64 | kTransB, 1);
           mma_commit(bX);
         }
-        // O1 = Q S^T into [token lane][dv column] (single BF16: the output is
-        // BF16). M = 128: rows 64-127 of the A operand are the K tile that
-        // follows Q in shared memory, results unused. The row warps must have
-        // read the previous chunk's outputs.
+        // O1^T = S Q^T into [dv lane][token column] (single BF16: the output
+        // is BF16). The row warps must have read the previous chunk's outputs.
         ok = wait(bQ, par) && ok;
         if (ci > 0) ok = wait(bOr, (ci - 1) & 1) && ok;
         fence_after_sync();
         if (ok) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16(taddr + 256, tile_desc(qt, 128, kk), tile_desc(sah, 128, kk), id128, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 384, sah + 8 * kk, tile_desc(qt, 128, kk), id64, kk > 0);
           mma_commit(bO1);
           last = bO1;
           last_par = par;
         }
-        // S += (Delta^T D) K (hi and lo passes);  O2 = P Delta (rows 64-127
-        // of the A operand: the 8 KB after P, results unused).
+        // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
         ok = wait(bDr, par);
         ok = wait(bK, par) && ok;
         ok = wait(bP, par) && ok;
         fence_after_sync();
         if (ok) {
           const uint32_t idk = id128 | kTransB;
-          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddh, 64, kk), mn_desc(kt, 128, kk), idk, 1);
-          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr, tile_desc(ddl, 64, kk), mn_desc(kt, 128, kk), idk, 1);
+          // A operands in TMEM: tokens 0-31 of each part in the hf = 0 columns,
+          // tokens 32-63 in the hf = 1 columns (32 further on).
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(256, kk), mn_desc(kt, 128, kk), idk, 1);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(272, kk), mn_desc(kt, 128, kk), idk, 1);
           mma_commit(bS);
-          for (int kk = 0; kk < 4; ++kk) mma_bf16(taddr + 384, tile_desc(p, 64, kk), tile_desc(da, 64, kk), id128, kk > 0);
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr + 448, dcol(320, kk), tile_desc(p, 64, kk), id64, kk > 0);
           mma_commit(bO);
           last = bO;
           last_par = par;
@@ -720,41 +719,43 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       tmem_st32(tmem_warp_addr(taddr, c0), vbuf);
     }
     auto row_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r. The threads of
-    // warps 0, 1, 4 and 5 (lanes 0-63: token = row) read 64 consecutive
-    // outputs of their token (dv from 64 hf) and stage them in the Delta^T
-    // tile (free until this chunk's Delta: the previous chunk's O2 has read
-    // it), 256 bytes per token with its 16-byte chunks XOR-swizzled by the
-    // token; once every row thread has released the accumulators, all of them
-    // write the staged rows out as whole 256-byte rows of o (16 lanes per
-    // row), so that each warp store covers four full lines.
-    auto write_outputs = [&](int cj) {
-      const int c0 = start + cj * kC;
-      const int n = min(kC, end - c0);
+    // Outputs of chunk cj: o_r = e^{g_r} rq_r O1_r + O2_r, in two parts.
+    // stage_outputs: row thread (i, hf) holds output dv = i of tokens
+    // [32 hf, 32 hf + 32); it releases the accumulators and stages the values
+    // as [token][dv] BF16, 256 bytes per token with its 16-byte chunks
+    // XOR-swizzled by the token (a warp's stores for one token fill 64
+    // contiguous bytes). copy_outputs, after the next Delta (so that it
+    // overlaps the S update instead of the X products) and a barrier of the
+    // row threads: all of them write the staged rows out as whole 256-byte
+    // rows of o (16 lanes per row), so that each warp store covers four full
+    // lines.
+    unsigned char* stg = sm + kS2_STG;
+    auto stage_outputs = [&](int cj) {
       wait(bO, cj & 1);
       __syncwarp();
       fence_after_sync();
-      unsigned char* stg = sm + kS2_DA;
-      if ((warp & 3) < 2) {
-        const float qr = qs[64 * (cj & 1) + row];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float o1[32], o2[32];
-          tmem_ld32x2(tmem_warp_addr(taddr, 256 + 64 * hf + 32 * half),
-                      tmem_warp_addr(taddr, 384 + 64 * hf + 32 * half), o1, o2);
-#pragma unroll
-          for (int e8 = 0; e8 < 4; ++e8) {
-            float v8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v8[e] = fmaf(o1[8 * e8 + e], qr, o2[8 * e8 + e]);
-            const int j = 8 * hf + 4 * half + e8;
-            *reinterpret_cast<uint4*>(stg + row * 256 + ((j ^ (row & 15)) << 4)) = pack8(v8);
-          }
-        }
-      }
+      float o1[32], o2[32];
+      tmem_ld32x2(tmem_warp_addr(taddr, 384 + 32 * hf), tmem_warp_addr(taddr, 448 + 32 * hf), o1, o2);
       fence_before_sync();
       mbar_arrive(bOr);
-      row_sync();
+      const float4* qv = reinterpret_cast<const float4*>(qs + 64 * (cj & 1) + 32 * hf);
+      const int jc = row >> 3, jb = (row & 7) * 2;
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 q4 = qv[e4];
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 32 * hf + 4 * e4 + e;
+          *reinterpret_cast<__nv_bfloat16*>(stg + r * 256 + ((jc ^ (r & 15)) << 4) + jb) =
+              __float2bfloat16_rn(fmaf(o1[4 * e4 + e], qq[e], o2[4 * e4 + e]));
+        }
+      }
+    };
+    auto copy_outputs = [&](int cj) {
+      const int c0 = start + cj * kC;
+      const int n = min(kC, end - c0);
+      row_sync();   // every thread's staging is written
       if (!failed()) {
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
@@ -764,7 +765,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                 *reinterpret_cast<const uint4*>(stg + t * 256 + ((j ^ (t & 15)) << 4));
         }
       }
-      row_sync();   // the staging is read before Delta overwrites it
+      // The next stage_outputs comes after the next chunk's first row
+      // barrier, so the staging is read before it is overwritten.
     };
 
     for (int ci = 0; ci < nchunks && records_ok; ++ci) {
@@ -773,9 +775,9 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       const uint32_t par = ci & 1;
       // Once the previous chunk's S update is done, so are every row
       // thread's reads of the gate buffers this chunk refills (Delta two
-      // chunks ago, the outputs staged in the previous chunk). The record's
-      // gates are refilled only after this chunk's X MMAs, which wait for the
-      // S tiles below.
+      // chunks ago, the outputs of two chunks ago), and the MMAs that read
+      // the previous S hi/lo parts. The record's gates are refilled only
+      // after this chunk's X MMAs, which wait for the S parts below.
       if (ci > 0) wait(bS, (ci - 1) & 1);
       wait(bW, par);
       const float glast = gk[n - 1];
@@ -786,7 +788,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         dkb[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
         qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
       }
-      // (b) this thread's half of S row i -> hi/lo A tiles, then S <- e^{g_last} S.
+      // (b) this thread's half of S row i -> BF16 hi/lo pairs in TMEM (the
+      // X and O1 MMAs' A operands), then S <- e^{g_last} S.
       __syncwarp();
       fence_after_sync();
       {
@@ -794,16 +797,18 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         float s0[32], s1[32];
         tmem_ld32x2(tmem_warp_addr(taddr, cb0), tmem_warp_addr(taddr, cb1), s0, s1);
 #pragma unroll
-        for (int e8 = 0; e8 < 4; ++e8) {
-          uint4 hi, lo;
-          split8(s0 + 8 * e8, hi, lo);
-          *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb0 + 8 * e8, 128)) = hi;
-          *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb0 + 8 * e8, 128)) = lo;
-          split8(s1 + 8 * e8, hi, lo);
-          *reinterpret_cast<uint4*>(sm + kS2_SAH + tile_off(row, cb1 + 8 * e8, 128)) = hi;
-          *reinterpret_cast<uint4*>(sm + kS2_SAL + tile_off(row, cb1 + 8 * e8, 128)) = lo;
+        for (int part = 0; part < 2; ++part) {
+          const float* sv = part ? s1 : s0;
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            hi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+            lo[e] = pack_bf16x2(sv[2 * e] - bf16lo(hi[e]), sv[2 * e + 1] - bf16hi(hi[e]));
+          }
+          // dk j = 64 hf + 32 part + 2 e + {0, 1} -> column j / 2
+          tmem_st16x2(tmem_warp_addr(taddr, 128 + 32 * hf + 16 * part),
+                      tmem_warp_addr(taddr, 192 + 32 * hf + 16 * part), hi, lo);
         }
-        fence_smem_to_async();
         fence_before_sync();
         mbar_arrive(bSr);
         // S <- e^{g_last} S, off the X MMAs' path: only this chunk's S update
@@ -816,46 +821,57 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         tmem_st32x2(tmem_warp_addr(taddr, cb0), tmem_warp_addr(taddr, cb1), s0, s1);
       }
       row_sync();   // dks and qs are written before they are read
-      // The previous chunk's outputs while this chunk's X MMAs run.
-      if (ci > 0) write_outputs(ci - 1);
+      // The previous chunk's outputs released and staged while this chunk's
+      // X MMAs run.
+      if (ci > 0) stage_outputs(ci - 1);
       // (d) Delta^T = U^T - X^T for row i, tokens [32 hf, 32 hf + 32).
       wait(bX, par);
       __syncwarp();
       fence_after_sync();
       {
         float xv[32], xl[32];
-        tmem_ld32x2(tmem_warp_addr(taddr, 128 + 32 * hf), tmem_warp_addr(taddr, 192 + 32 * hf),
+        tmem_ld32x2(tmem_warp_addr(taddr, 256 + 32 * hf), tmem_warp_addr(taddr, 320 + 32 * hf),
                     xv, xl);
 #pragma unroll
         for (int e = 0; e < 32; ++e) xv[e] += xl[e];
         wait(bU, par);
+        // Delta and (Delta D) hi / lo as BF16 pairs of consecutive tokens,
+        // written over this thread's own X columns (already read): (Delta D)
+        // hi at [256 + 32 hf, + 16), lo at [272 + 32 hf, + 16), Delta at
+        // [320 + 32 hf, + 16); the MMAs read them as A operands (K = tokens).
+        uint32_t dl[16], dh[16], dlo[16];
 #pragma unroll
         for (int e8 = 0; e8 < 4; ++e8) {
           const float4 u0 = us[row * 16 + ((8 * hf + 2 * e8) ^ (row & 7))];
           const float4 u1 = us[row * 16 + ((8 * hf + 2 * e8 + 1) ^ (row & 7))];
           const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-          float dl[8], dd[8];
+          float del[8], dd[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int r = 32 * hf + 8 * e8 + e;
-            const float del = r < n ? uu[e] - xv[8 * e8 + e] : 0.f;
-            dl[e] = del;
-            dd[e] = del * dkb[r];
+            del[e] = r < n ? uu[e] - xv[8 * e8 + e] : 0.f;
+            dd[e] = del[e] * dkb[r];
           }
-          const int s0 = 32 * hf + 8 * e8;
-          uint4 hi, lo;
-          *reinterpret_cast<uint4*>(sm + kS2_DA + tile_off(row, s0, 64)) = pack8(dl);
-          split8(dd, hi, lo);
-          *reinterpret_cast<uint4*>(sm + kS2_DDH + tile_off(row, s0, 64)) = hi;
-          *reinterpret_cast<uint4*>(sm + kS2_DDL + tile_off(row, s0, 64)) = lo;
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            dl[4 * e8 + e2] = pack_bf16x2(del[2 * e2], del[2 * e2 + 1]);
+            const uint32_t hv = pack_bf16x2(dd[2 * e2], dd[2 * e2 + 1]);
+            dh[4 * e8 + e2] = hv;
+            dlo[4 * e8 + e2] = pack_bf16x2(dd[2 * e2] - bf16lo(hv), dd[2 * e2 + 1] - bf16hi(hv));
+          }
         }
+        tmem_st16x2(tmem_warp_addr(taddr, 256 + 32 * hf), tmem_warp_addr(taddr, 272 + 32 * hf), dh,
+                    dlo);
+        tmem_st16(tmem_warp_addr(taddr, 320 + 32 * hf), dl);
       }
-      fence_smem_to_async();
       fence_before_sync();
       mbar_arrive(bDr);
+      if (ci > 0) copy_outputs(ci - 1);
     }
     if (records_ok && nchunks > 0) {
-      write_outputs(nchunks - 1);
+      row_sync();   // the last copy_outputs is done with the staging
+      stage_outputs(nchunks - 1);
+      copy_outputs(nchunks - 1);
       wait(bS, (nchunks - 1) & 1);
       __syncwarp();
       fence_after_sync();

@@ -93,6 +93,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] x B[smem desc]^T: A in tensor memory, row m in lane m
+// and its K elements as consecutive BF16 pairs along the columns (element k in
+// column k / 2, the lower half for even k), so that one K = 16 step reads 8
+// columns starting at a_tmem.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive (once) on the mbarrier when all previously issued MMAs complete.
 __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
   asm volatile(
@@ -279,6 +292,35 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va
     va[i] = __uint_as_float(r[i]);
     vb[i] = __uint_as_float(r[32 + i]);
   }
+}
+
+// Two 16-column stores of raw 32-bit words and one wait.
+__device__ __forceinline__ void tmem_st16x2(uint32_t ta, uint32_t tb, const uint32_t (&va)[16],
+                                            const uint32_t (&vb)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], "
+      "{%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(ta), "r"(tb), "r"(va[0]), "r"(va[1]), "r"(va[2]), "r"(va[3]), "r"(va[4]),
+         "r"(va[5]), "r"(va[6]), "r"(va[7]), "r"(va[8]), "r"(va[9]), "r"(va[10]), "r"(va[11]),
+         "r"(va[12]), "r"(va[13]), "r"(va[14]), "r"(va[15]), "r"(vb[0]), "r"(vb[1]), "r"(vb[2]),
+         "r"(vb[3]), "r"(vb[4]), "r"(vb[5]), "r"(vb[6]), "r"(vb[7]), "r"(vb[8]), "r"(vb[9]),
+         "r"(vb[10]), "r"(vb[11]), "r"(vb[12]), "r"(vb[13]), "r"(vb[14]), "r"(vb[15])
+      : "memory");
+}
+
+// One 16-column store of raw 32-bit words and its wait.
+__device__ __forceinline__ void tmem_st16(uint32_t ta, const uint32_t (&va)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;"
+      :: "r"(ta), "r"(va[0]), "r"(va[1]), "r"(va[2]), "r"(va[3]), "r"(va[4]), "r"(va[5]),
+         "r"(va[6]), "r"(va[7]), "r"(va[8]), "r"(va[9]), "r"(va[10]), "r"(va[11]), "r"(va[12]),
+         "r"(va[13]), "r"(va[14]), "r"(va[15])
+      : "memory");
 }
 
 // Two 32-column stores and one wait.
