@@ -1,7 +1,6 @@
 // C ABI of the GDN hot path: host-side argument validation, then the kernel
 // launchers. Nothing here allocates device memory or synchronises.
 #include <cstring>
-#include <mutex>
 #include <string>
 
 #include "gdn_internal.cuh"
@@ -9,18 +8,18 @@
 
 namespace gdn {
 namespace {
-std::mutex g_err_mu;
-std::string g_err_text;
+// Text of the calling thread's most recent CUDA failure (like errno: a pointer
+// returned to one thread is never invalidated by another thread's failure).
+thread_local std::string t_err_text;
 constexpr int kConvTaps = 4;
 
 bool head_dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 }  // namespace
 
 void set_cuda_error(cudaError_t e) {
-  std::lock_guard<std::mutex> lock(g_err_mu);
-  g_err_text = cudaGetErrorName(e);
-  g_err_text += ": ";
-  g_err_text += cudaGetErrorString(e);
+  t_err_text = cudaGetErrorName(e);
+  t_err_text += ": ";
+  t_err_text += cudaGetErrorString(e);
 }
 }  // namespace gdn
 
@@ -63,10 +62,7 @@ const char* gdn_status_string(gdn_status_t s) {
   return "GDN: unknown status";
 }
 
-const char* gdn_last_cuda_error_string(void) {
-  std::lock_guard<std::mutex> lock(g_err_mu);
-  return g_err_text.c_str();
-}
+const char* gdn_last_cuda_error_string(void) { return t_err_text.c_str(); }
 
 gdn_status_t gdn_build_conv_chunks(const int32_t* cu_seqlens, int32_t num_seqs,
                                    int32_t chunk_tokens, gdn_conv_chunk_t* chunks,

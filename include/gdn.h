@@ -376,8 +376,9 @@ GDN_API gdn_status_t gdn_selftest_bounded_wait(int32_t* device_status, int64_t m
 /* Static description of a status code (never NULL). */
 GDN_API const char* gdn_status_string(gdn_status_t status);
 
-/* Text of the CUDA error behind the most recent GDN_ERR_CUDA in this process
- * ("" if none). The pointer stays valid until the next failing call. */
+/* Text of the CUDA error behind the calling thread's most recent GDN_ERR_CUDA
+ * ("" if none). Kept per thread, like errno: the pointer stays valid until the
+ * same thread's next failing call, whatever other threads do. */
 GDN_API const char* gdn_last_cuda_error_string(void);
 
 #ifdef __cplusplus
