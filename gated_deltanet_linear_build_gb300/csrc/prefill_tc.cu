@@ -455,14 +455,16 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 //   warps 0-7 (rows): warp w owns TMEM lanes 32 (w % 4) .. + 31 (row i of S)
 //     and column half w / 4. Per chunk: S -> BF16 hi/lo parts (in TMEM) and
 //     S <- e^{g_last} S; the previous chunk's outputs; Delta = U - X.
-//   warp 8 (one lane): the MMAs. X^T = S W^T (hi/lo) and O1^T = S Q^T once
-//     the S parts are ready (A operands read from TMEM, so S costs no shared
+//   warp 8 (one lane): the recurrence's MMAs. X^T = S W^T (hi/lo) once the
+//     S parts are ready (A operands read from TMEM, so S costs no shared
 //     memory traffic); S += (Delta^T D) K (hi/lo) and O2^T = Delta^T P^T
 //     once Delta is.
 //   warp 9: the next chunk's record (W and gates, U, P) by bulk copies, each
 //     as soon as the buffer it refills is free.
 //   warps 10 and 11: the next chunk's raw Q and K rows (16-byte asynchronous
-//     copies by all lanes) once the previous tile's readers are done.
+//     copies by all lanes) once the previous tile's readers are done; warp 10
+//     also issues O1^T = S Q^T, so that the recurrence's MMA lane never waits
+//     on the output products.
 // TMEM: S [0, 128), S hi [128, 192) and S lo [192, 256) as BF16 pairs (dk j
 // in column j / 2), X^T [256, 384) (two partial sums; once read, the Delta
 // parts as BF16 pairs of tokens), O1^T [384, 448) and O2^T [448, 512) (dv i
@@ -501,7 +503,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   uint64_t* bSr = bars + 5;   // S hi/lo parts written     (256 row threads)
   uint64_t* bDr = bars + 6;   // Delta tiles written       (256 row threads)
   uint64_t* bX = bars + 7;    // X MMAs done               (commit)
-  uint64_t* bO1 = bars + 8;   // O1 MMAs done              (commit)
+  uint64_t* bO1 = bars + 8;   // O1 MMAs done              (commit, warp 10)
   uint64_t* bS = bars + 9;    // S update done             (commit)
   uint64_t* bO = bars + 10;   // O2 MMAs (and all before) done (commit)
   uint64_t* bOr = bars + 11;  // outputs read from TMEM    (256 row threads)
@@ -592,15 +594,46 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     fence_smem_to_async();
     mbar_arrive(bar);
   };
-  if (warp == 10 || warp == 11) {
-    // ---------------- Q rows (warp 10) or K rows (warp 11) ----------------
-    const bool is_q = warp == 10;
+  if (warp == 10) {
+    // ---------------- Q rows and the O1 products (warp 10) ----------------
+    // O1^T = S Q^T into [dv lane][token column] (single BF16: the output is
+    // BF16), issued here, beside the recurrence's MMAs, once the chunk's Q
+    // rows and S parts are in place and the row warps have read the previous
+    // chunk's outputs; Q is reloaded once O1 has read it.
+    bool issued = false;
+    uint32_t last_par = 0;
     if (records_ok) {
-      rows(0, is_q ? q : k, is_q ? kS2_Q : kS2_K, is_q ? bQ : bK);
+      const uint32_t id64 = idesc_bf16_f32(128, 64);
+      const uint32_t sah = taddr + 128, qt = smem_u32(sm + kS2_Q);
+      for (int ci = 0; ci < nchunks; ++ci) {
+        const uint32_t par = ci & 1;
+        if (ci > 0 && !wait(bO1, (ci - 1) & 1)) break;
+        rows(ci, q, kS2_Q, bQ);
+        bool ok = wait(bQ, par);
+        ok = wait(bSr, par) && ok;
+        if (ci > 0) ok = wait(bOr, (ci - 1) & 1) && ok;
+        __syncwarp();
+        fence_after_sync();
+        if (ok && lane == 0) {
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 384, sah + 8 * kk, tile_desc(qt, 128, kk), id64, kk > 0);
+          mma_commit(bO1);
+          issued = true;
+          last_par = par;
+        }
+        __syncwarp();
+        if (!ok) break;
+      }
+    }
+    // Bounded, not abortable: the MMAs in flight must finish before exit.
+    if (lane == 0 && issued) mbar_wait(bO1, last_par);
+    __syncwarp();
+  } else if (warp == 11) {
+    // ---------------- K rows (warp 11) ----------------
+    if (records_ok) {
+      rows(0, k, kS2_K, bK);
       for (int ci = 0; ci + 1 < nchunks; ++ci) {
-        // Q is free once the chunk's O1 has read it, K once its S update has.
-        if (wait(is_q ? bO1 : bS, ci & 1))
-          rows(ci + 1, is_q ? q : k, is_q ? kS2_Q : kS2_K, is_q ? bQ : bK);
+        // K is free once the chunk's S update has read it.
+        if (wait(bS, ci & 1)) rows(ci + 1, k, kS2_K, bK);
       }
     }
     __syncwarp();
@@ -651,7 +684,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (lane == 0 && records_ok) {
       const uint32_t id64 = idesc_bf16_f32(128, 64), id128 = idesc_bf16_f32(128, 128);
       const uint32_t sah = taddr + 128, sal = taddr + 192;   // S hi / lo in TMEM
-      const uint32_t w = smem_u32(sm + kS2_W), qt = smem_u32(sm + kS2_Q);
+      const uint32_t w = smem_u32(sm + kS2_W);
       const uint32_t p = smem_u32(sm + kS2_P), kt = smem_u32(sm + kS2_K);
       // TMEM column of K step kk (16 tokens) of a Delta part based at `col`
       auto dcol = [&](int col, int kk) { return taddr + col + 8 * kk + (kk >= 2 ? 16 : 0); };
@@ -669,17 +702,6 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sah + 8 * kk, mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
           for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sal + 8 * kk, mn_desc(w, 128, kk), id64 | kTransB, 1);
           mma_commit(bX);
-        }
-        // O1^T = S Q^T into [dv lane][token column] (single BF16: the output
-        // is BF16). The row warps must have read the previous chunk's outputs.
-        ok = wait(bQ, par) && ok;
-        if (ci > 0) ok = wait(bOr, (ci - 1) & 1) && ok;
-        fence_after_sync();
-        if (ok) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 384, sah + 8 * kk, tile_desc(qt, 128, kk), id64, kk > 0);
-          mma_commit(bO1);
-          last = bO1;
-          last_par = par;
         }
         // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
         ok = wait(bDr, par);
@@ -731,6 +753,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     // lines.
     unsigned char* stg = sm + kS2_STG;
     auto stage_outputs = [&](int cj) {
+      wait(bO1, cj & 1);
       wait(bO, cj & 1);
       __syncwarp();
       fence_after_sync();
@@ -804,6 +827,13 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           for (int e = 0; e < 16; ++e) {
             hi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
             lo[e] = pack_bf16x2(sv[2 * e] - bf16lo(hi[e]), sv[2 * e + 1] - bf16hi(hi[e]));
+          }
+          // The previous chunk's O1 (issued by warp 10) reads S hi until its
+          // commit.
+          if (part == 0 && ci > 0) {
+            wait(bO1, (ci - 1) & 1);
+            __syncwarp();
+            fence_after_sync();
           }
           // dk j = 64 hf + 32 part + 2 e + {0, 1} -> column j / 2
           tmem_st16x2(tmem_warp_addr(taddr, 128 + 32 * hf + 16 * part),
