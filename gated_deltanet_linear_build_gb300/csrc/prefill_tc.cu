@@ -2,12 +2,14 @@
 // (tcgen05, accumulators in TMEM), head dimension 128.
 //
 // The chunk algebra is the one described in prefill.cu. Everything is laid out
-// so that every product has M = 128 (the head dimension) and K-major operands:
+// so that every product has M = 128 (the head dimension); operand tiles use the
+// K-major and MN-major layouts described in tc_ptx.cuh, or TMEM for A:
 //
 //   chunk kernel, one CTA per (64-token chunk, v-head):
 //     G    = [K; Q] K^T                        (M=128: K rows then Q rows, N=64, K=128)
 //     A_rs = b_r e^{g_r-g_s} (k_r.k_s), P_rs = e^{g_r-g_s} (q_r.k_s)     (CUDA cores)
-//     Tm   = (I + A)^{-1}: one column per thread, forward substitution  (CUDA cores)
+//     Tm   = (I + A)^{-1}: 16 x 16 diagonal blocks by forward substitution,
+//            the blocks below them by blocked products          (CUDA cores)
 //     W^T  = K^T (Tm diag(b e^g))^T,  U^T = V^T (Tm diag(b))^T          (M=128, N=64, K=64)
 //   and writes, per (chunk, v-head), a record with W (BF16 hi + lo) and P (in
 //   the tile layouts the state kernel feeds straight to the tensor core), U
@@ -449,8 +451,8 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 
 // ---------------------------------------------------------------------------
 // State kernel: one CTA per (sequence, v-head), S [dv = 128 x dk = 128]
-// float32 resident in TMEM, chunks in order. Three warp roles hand work to
-// each other through mbarriers only, so that no role waits for another's
+// float32 resident in TMEM, chunks in order. The warp roles hand work to each
+// other through mbarriers only, so that no role waits for another's
 // instruction stream:
 //   warps 0-7 (rows): warp w owns TMEM lanes 32 (w % 4) .. + 31 (row i of S)
 //     and column half w / 4. Per chunk: S -> BF16 hi/lo parts (in TMEM) and
