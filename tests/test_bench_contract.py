@@ -1,0 +1,113 @@
+"""bench.py's JSON contract, roofline units and measurement hygiene, on the CPU.
+
+- The algorithmic work per launch, which every roofline fraction divides by, is
+  checked against counts taken from the tensor shapes of the workload.
+- Stored ncu DRAM traffic is reported only while the kernel's source is the one
+  it was captured from.
+- The clock summary flags throttle reasons from nvidia-smi's CSV.
+- The reference arm (the oracle timed on host cores) prints one line with the
+  contract's keys.
+
+No GPU is used. The oracle's timing sample is replaced by fixed timings, so no
+oracle arithmetic runs here.
+"""
+import hashlib
+import json
+
+import pytest
+
+import bench
+
+
+def test_decode_bytes_count():
+    # One decode launch of the mix: 32 sequences x 32 v-heads (16 k-heads), d = 128.
+    n, hv, hk, d = 32, 32, 16, 128
+    state = n * hv * d * d * 4 * 2          # S float32, read and written once
+    inputs = n * (2 * hk * d + hv * d) * 2  # q, k (per k-head) and v, BF16
+    gates = n * hv * 4 * 2                  # a and b, float32
+    out = n * hv * d * 2                    # o, BF16
+    assert bench.decode_delta_bytes(n) == state + inputs + gates + out == 135_012_352
+
+
+def test_conv_bytes_count():
+    C = 8192
+    # 2048-token step of 2 sequences: x in, y out (BF16), taps [C, 4], state [2, C, 3] in + out.
+    assert bench.conv_prefill_bytes(2048, 2) == 2048 * C * 2 * 2 + C * 4 * 2 + 2 * C * 3 * 2 * 2
+    # 32-sequence decode step: x in, y out, state in + out, taps.
+    assert bench.conv_update_bytes(32) == 32 * C * 2 * 2 + 32 * C * 3 * 2 * 2 + C * 4 * 2
+    assert bench.conv_update_bytes(32) == 4_259_840
+
+
+def test_prefill_flops_per_chunk_head():
+    # A full 64-token chunk of one head at d = 128 is about 11.6 MFLOP; the
+    # count is additive over chunks and heads, and a partial chunk costs less.
+    one = bench.prefill_flops([64], d=128, hv=1)
+    assert 11.6e6 < one < 11.7e6
+    assert bench.prefill_flops([64] * 32, d=128, hv=32) == pytest.approx(32 * 32 * one)
+    assert bench.prefill_flops([13], d=128, hv=1) < one
+    # Chunks of one token: 5 d + 3 d^2 + 1/6 MACs, twice for flops.
+    assert bench.prefill_flops([1], d=128, hv=1) == pytest.approx(2 * (5 * 128 + 3 * 128 * 128 + 1 / 6))
+
+
+def test_stored_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    src = tmp_path / "kernel.cu"
+    src.write_text("__global__ void k() {}\n")
+    (tmp_path / "profiles").mkdir()
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(
+        {"delta_decode": {"source": "kernel.cu", "source_sha256_16": digest,
+                          "dram_bytes_per_launch": 123.0}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.stored_traffic("delta_decode") == 123.0
+    assert bench.stored_traffic("conv_prefill") is None
+    src.write_text("__global__ void k() { /* changed */ }\n")
+    assert bench.stored_traffic("delta_decode") is None
+
+
+def test_committed_traffic_matches_the_decode_source():
+    # The committed capture belongs to the decode kernel as it is now.
+    assert bench.stored_traffic("delta_decode") is not None
+
+
+def test_clock_summary_flags_throttle_reasons():
+    s = bench.ClockSampler(0)
+    s.lines = [
+        "2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "2055, 2070, 1390.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+        "1980, 2070, 1399.0, 0x0000000000000020, Not Active, Active, Not Active, Active",
+    ]
+    out = s.summary()
+    assert out["samples"] == 3
+    assert out["sm_mhz"] == 2055.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler(0).summary()["samples"] == 0
+
+
+def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
+    calls = []
+
+    def fake_sample(seconds):
+        calls.append(seconds)
+        return 2e-3, 5e-4, 0.0            # oracle seconds per decode / prefill token-layer
+
+    monkeypatch.setattr(bench, "cpu_oracle_sample", fake_sample)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1"]) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert rec["impl"] == "reference" and rec["steps"] == 2 and rec["warmup"] == 1
+    assert len(calls) == 3                # one warm-up sample, then one per timed step
+    from gated_deltanet_linear_build_gb300 import synth
+    pre = int(sum(int(x) for x in synth.serving_mix_lengths(bench.rank_lengths_seed(0))))
+    dec = bench.DECODE_STEPS * bench.N_SEQS
+    assert rec["value"] == pytest.approx(bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec))
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
