@@ -5,7 +5,6 @@ No test here reaches a kernel launch: every call either fails validation or
 has nothing to do, so these run without a GPU. Fake pointer values are never
 dereferenced on those paths.
 """
-import ctypes
 import os
 import re
 

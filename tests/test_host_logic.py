@@ -3,7 +3,6 @@ path, on the CPU (no GPU, gloo for the 2-rank case)."""
 import os
 import socket
 
-import numpy as np
 import pytest
 import torch
 import torch.distributed as dist
