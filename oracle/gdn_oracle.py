@@ -185,6 +185,21 @@ def l2norm(x, eps: float = L2NORM_EPS):
     return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
 
 
+def gate_activation(z_a, z_b):
+    """Decay and write strength from raw gate logits (float64):
+        a = exp(-softplus(z_a)) = 1 / (1 + e^{z_a}),   b = sigmoid(z_b) = 1 / (1 + e^{-z_b}),
+    softplus(z) = log(1 + e^z) taken as logaddexp(0, z) so that large z does
+    not overflow. The GDN gate prep between the conv and the recurrence
+    ("RTX 5070 Ti: close Qwen3.5-4B TTFT, TPOT, and VRAM gaps vs vLLM",
+    Existing evidence: the post-conv tile).
+    """
+    z_a = np.asarray(z_a, np.float64)
+    z_b = np.asarray(z_b, np.float64)
+    a = np.exp(-np.logaddexp(0.0, z_a))
+    b = np.exp(-np.logaddexp(0.0, -z_b))
+    return a, b
+
+
 def _head_map(hk: int, hv: int) -> np.ndarray:
     """q/k-head read by each v-head: contiguous groups of hv // hk v-heads."""
     return np.arange(hv) // (hv // hk)
@@ -355,11 +370,16 @@ def delta_rule_prefill_chunked(q_bits, k_bits, v_bits, a, b, cu_seqlens, S0,
 
 
 # ----------------------------------------------------------------------------
-# Comparison metric used by every parity check
+# Comparison metrics used by the parity checks
 # ----------------------------------------------------------------------------
 
 def rel_err(x, ref) -> float:
-    """max |x - ref| / max |ref| over the tensor (0 when both are all zero)."""
+    """max |x - ref| / max |ref| over the tensor (0 when both are all zero).
+
+    Both maxima are of absolute values, and the denominator is the
+    reference's, not the candidate's. When the reference is all zero the
+    absolute error max |x| is returned.
+    """
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     den = np.max(np.abs(ref)) if ref.size else 0.0
@@ -367,6 +387,34 @@ def rel_err(x, ref) -> float:
     if den == 0.0:
         return float(num)
     return float(num / den)
+
+
+def rel_err_slices(x, ref, slice_ndim: int, floor: float = 0.0) -> float:
+    """The largest ``rel_err`` over the slices formed by the last ``slice_ndim``
+    axes (one slice per index of the leading axes).
+
+    Each slice is measured against its own scale max |ref_slice|, floored at
+    ``floor`` times the scale of the whole tensor, so that a slice whose
+    reference is (nearly) zero is measured against the tensor's magnitude
+    instead of being divided by zero. With ``floor = 0`` a slice whose
+    reference is all zero contributes its absolute error, as ``rel_err``.
+    Used with one output row per (token, head) and one state per
+    (sequence, head), so that a small-magnitude head cannot hide behind a
+    large one.
+    """
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return 0.0
+    lead = ref.shape[:ref.ndim - slice_ndim]
+    n = int(np.prod(lead)) if lead else 1
+    xs = x.reshape(n, -1)
+    rs = ref.reshape(n, -1)
+    num = np.max(np.abs(xs - rs), axis=1)
+    den = np.max(np.abs(rs), axis=1)
+    den = np.maximum(den, floor * float(np.max(np.abs(rs))))
+    out = np.where(den > 0.0, num / np.where(den > 0.0, den, 1.0), num)
+    return float(np.max(out))
 
 
 # ----------------------------------------------------------------------------
@@ -393,20 +441,26 @@ def rms_norm_bf16(h):
     return to_bf16(h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + RMS_EPS))
 
 
-def _gates(x_vals, u, r, hk, hv, d):
+def _gate_logits(x_vals, u, r, hk, hv, d):
+    """Gate logits of the synthetic stack: z_a[h] = u_h . x_v[h] / sqrt(d) and
+    z_b[h] = r_h . x_v[h] / sqrt(d), with x_v[h] the pre-conv v slice of head h."""
     xv = x_vals[:, 2 * hk * d:].reshape(-1, hv, d)
     za = np.einsum("lhd,hd->lh", xv, np.asarray(u, np.float64)) / np.sqrt(d)
     zb = np.einsum("lhd,hd->lh", xv, np.asarray(r, np.float64)) / np.sqrt(d)
-    a = np.exp(-np.logaddexp(0.0, za)).astype(np.float32)
-    b = (1.0 / (1.0 + np.exp(-zb))).astype(np.float32)
-    return a, b
+    return za, zb
 
 
-def _stack_layer(stack, l, h, carry, first: bool, chunk: int):
+def _gates(x_vals, u, r, hk, hv, d):
+    za, zb = _gate_logits(x_vals, u, r, hk, hv, d)
+    a, b = gate_activation(za, zb)
+    return a.astype(np.float32), b.astype(np.float32)
+
+
+def _stack_layer(stack, l, h, carry, first: bool):
     """Layer l of the synthetic stack on rows h [T, C] of ONE sequence.
 
-    first: the rows are the whole prompt (conv prefill and chunked delta rule
-    from zero state); otherwise h holds one decode token. carry["conv"][l] and
+    first: the rows are the whole prompt (conv prefill and the delta rule token
+    by token from zero state); otherwise h holds one decode token. carry["conv"][l] and
     carry["S"][l] are read and replaced. Returns the new residual stream rows.
     """
     hk, hv, d = stack["hk"], stack["hv"], stack["d"]
@@ -423,8 +477,8 @@ def _stack_layer(stack, l, h, carry, first: bool, chunk: int):
     k = yb[:, hk * d:2 * hk * d].reshape(T, hk, d)
     v = yb[:, 2 * hk * d:].reshape(T, hv, d)
     if first:
-        o, carry["S"][l] = delta_rule_prefill_chunked(q, k, v, a, b, [0, T], carry["S"][l], [0],
-                                                      qk_l2norm=True, chunk=chunk)
+        o, carry["S"][l] = delta_rule_prefill(q, k, v, a, b, [0, T], carry["S"][l], [0],
+                                              qk_l2norm=True)
     else:
         o, carry["S"][l] = delta_rule_decode(q, k, v, a, b, carry["S"][l], qk_l2norm=True)
     ob = round_bf16(o).reshape(T, hv * d)
@@ -442,20 +496,20 @@ def stack_logits(stack, h_rows):
     return from_bf16(rms_norm_bf16(h_rows)) @ from_bf16(stack["head"])
 
 
-def serving_stack_sequence(stack, s: int, n_decode: int = 128, chunk: int = 64):
+def serving_stack_sequence(stack, s: int, n_decode: int = 128):
     """Greedy generation of sequence s through the synthetic stack.
 
     Prompt: ``stack["prompts"][s]``; returns (ids, margins, logits_rows): the
     n_decode + 1 generated ids, the top-1 minus top-2 logit margin at each, and
-    the logits rows (float64). The prompt goes through each layer at once
-    (chunked evaluation of the delta rule, pinned equal to the sequential
-    one); decode steps use the single-token forms.
+    the logits rows (float64). The prompt goes through each layer at once, the
+    delta rule token by token (the sequential recurrence, the definition);
+    decode steps use the single-token forms.
     """
     embed = from_bf16(stack["embed"])
     carry = _new_carry(stack)
     h = embed[np.asarray(stack["prompts"][s])]
     for l in range(stack["layers"]):
-        h = _stack_layer(stack, l, h, carry, True, chunk)
+        h = _stack_layer(stack, l, h, carry, True)
     ids, margins, rows = [], [], []
     lg = stack_logits(stack, h[-1:])[0]
     for step in range(n_decode + 1):
@@ -468,15 +522,15 @@ def serving_stack_sequence(stack, s: int, n_decode: int = 128, chunk: int = 64):
             break
         h = embed[[top]]
         for l in range(stack["layers"]):
-            h = _stack_layer(stack, l, h, carry, False, chunk)
+            h = _stack_layer(stack, l, h, carry, False)
         lg = stack_logits(stack, h)[0]
     return ids, margins, np.asarray(rows)
 
 
-def serving_stack_prefill_logits(stack, tokens, chunk: int = 64):
+def serving_stack_prefill_logits(stack, tokens):
     """Logits at every position of ``tokens`` run through the stack as one prompt."""
     carry = _new_carry(stack)
     h = from_bf16(stack["embed"])[np.asarray(tokens)]
     for l in range(stack["layers"]):
-        h = _stack_layer(stack, l, h, carry, True, chunk)
+        h = _stack_layer(stack, l, h, carry, True)
     return stack_logits(stack, h)

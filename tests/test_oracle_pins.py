@@ -221,6 +221,71 @@ def test_l2norm():
 
 
 # ----------------------------------------------------------------------------
+# a4: gate activation from raw logits
+# ----------------------------------------------------------------------------
+
+def test_gate_activation_by_hand():
+    # a = 1 / (1 + e^{z_a}), b = 1 / (1 + e^{-z_b}); z = ln 3 gives a = 1/4, b = 3/4.
+    za = np.array([0.0, np.log(3.0), -np.log(3.0)])
+    zb = np.array([0.0, np.log(3.0), -np.log(3.0)])
+    a, b = O.gate_activation(za, zb)
+    np.testing.assert_allclose(a, [0.5, 0.25, 0.75], rtol=1e-15)
+    np.testing.assert_allclose(b, [0.5, 0.75, 0.25], rtol=1e-15)
+
+
+def test_gate_activation_complementary_and_saturating():
+    # exp(-softplus(z)) = 1 - sigmoid(z): a(z) + b(z) = 1 for the same z.
+    z = np.linspace(-30.0, 30.0, 121)
+    a, b = O.gate_activation(z, z)
+    np.testing.assert_allclose(a + b, 1.0, rtol=0, atol=1e-15)
+    assert np.all(np.diff(a) < 0) and np.all(np.diff(b) > 0)
+    # no overflow at large |z|: the limits 0 and 1
+    a, b = O.gate_activation([1000.0, -1000.0], [1000.0, -1000.0])
+    assert a.tolist() == [0.0, 1.0] and b.tolist() == [1.0, 0.0]
+
+
+# ----------------------------------------------------------------------------
+# The parity metrics
+# ----------------------------------------------------------------------------
+
+def test_rel_err_by_hand():
+    assert O.rel_err([1.0, 2.0], [1.0, 2.0]) == 0.0
+    # the denominator is max|ref| (2), not max|x| (4)
+    assert O.rel_err([1.0, 4.0], [1.0, 2.0]) == 1.0
+    # absolute values in both maxima: a signed max would give 1 / 1 here
+    assert O.rel_err([-4.0, 2.0], [-4.0, 1.0]) == 0.25
+    # |x - ref|: a signed difference max would give 0 here
+    assert O.rel_err([1.0, -1.0], [1.0, 1.0]) == 2.0
+    # an all-zero reference: the absolute error
+    assert O.rel_err([0.0, 3e-3], [0.0, 0.0]) == 3e-3
+    assert O.rel_err([0.0, 0.0], [0.0, 0.0]) == 0.0
+    # a zero candidate against a non-zero reference: 1
+    assert O.rel_err([0.0, 0.0], [0.5, -2.0]) == 1.0
+    assert O.rel_err(np.zeros((0, 3)), np.zeros((0, 3))) == 0.0
+
+
+def test_rel_err_slices_by_hand():
+    ref = np.array([[[100.0, 0.0]], [[1.0, -1.0]]])     # two slices of shape [1, 2]
+    x = np.array([[[100.0, 0.5]], [[1.0, -1.5]]])
+    # whole tensor: 0.5 / 100; per slice: 0.5 / 100 and 0.5 / 1
+    assert O.rel_err(x, ref) == 0.005
+    assert O.rel_err_slices(x, ref, 2) == 0.5
+    assert O.rel_err_slices(x, ref, 1) == 0.5
+    # the floor: slice scale at least floor * max|ref| of the tensor
+    assert O.rel_err_slices(x, ref, 2, floor=0.1) == 0.05
+    # an all-zero slice without a floor: its absolute error
+    ref0 = np.array([[0.0, 0.0], [2.0, 2.0]])
+    x0 = np.array([[0.25, 0.0], [2.0, 2.0]])
+    assert O.rel_err_slices(x0, ref0, 1) == 0.25
+    assert O.rel_err_slices(x0, ref0, 1, floor=0.5) == 0.25
+    # one slice equals rel_err
+    rng = np.random.default_rng(3)
+    r = rng.standard_normal((4, 5))
+    c = r + 1e-3 * rng.standard_normal((4, 5))
+    assert O.rel_err_slices(c, r, 2) == O.rel_err(c, r)
+
+
+# ----------------------------------------------------------------------------
 # a5 / prefill: the delta rule
 # ----------------------------------------------------------------------------
 

@@ -61,7 +61,7 @@ def test_zero_residual_scale_reduces_to_a_bigram_map():
         return int(np.argmax(x @ W))
 
     for s in range(3):
-        ids, margins, _ = O.serving_stack_sequence(st, s, n_decode=5, chunk=4)
+        ids, margins, _ = O.serving_stack_sequence(st, s, n_decode=5)
         expect = [next_id(int(st["prompts"][s][-1]))]
         for _ in range(5):
             expect.append(next_id(expect[-1]))
@@ -81,7 +81,7 @@ def test_argmax_takes_the_first_of_equal_logits():
     # x has entries of both signs, so force a positive logit with x>0 rows:
     E = np.abs(O.from_bf16(st["embed"]))
     st["embed"] = O.to_bf16(E)
-    ids, margins, _ = O.serving_stack_sequence(st, 0, n_decode=3, chunk=4)
+    ids, margins, _ = O.serving_stack_sequence(st, 0, n_decode=3)
     assert ids == [3, 3, 3, 3]
     assert margins == [0.0] * 4
 
@@ -92,9 +92,9 @@ def test_prefill_then_decode_equals_one_longer_prefill(s):
     prompt to the decode forms, layer by layer) gives the logits that one
     prefill of prompt + generated[:-1] gives at the same positions."""
     st = tiny_stack()
-    ids, margins, rows = O.serving_stack_sequence(st, s, n_decode=6, chunk=4)
+    ids, margins, rows = O.serving_stack_sequence(st, s, n_decode=6)
     prompt = list(st["prompts"][s])
-    full = O.serving_stack_prefill_logits(st, prompt + ids[:-1], chunk=4)
+    full = O.serving_stack_prefill_logits(st, prompt + ids[:-1])
     L = len(prompt)
     assert np.max(np.abs(full[L - 1:] - rows)) <= 1e-9 * np.max(np.abs(rows))
     assert [int(np.argmax(r)) for r in full[L - 1:]] == ids
@@ -104,16 +104,16 @@ def test_stack_depends_on_every_layer():
     """Changing the last layer's conv weights changes the logits (no layer is
     skipped) while zeroing its residual scale removes its effect exactly."""
     st = tiny_stack()
-    _, _, rows = O.serving_stack_sequence(st, 1, n_decode=2, chunk=4)
+    _, _, rows = O.serving_stack_sequence(st, 1, n_decode=2)
     st2 = tiny_stack()
     st2["conv_w"][-1] = O.to_bf16(-O.from_bf16(st2["conv_w"][-1]))
-    _, _, rows2 = O.serving_stack_sequence(st2, 1, n_decode=2, chunk=4)
+    _, _, rows2 = O.serving_stack_sequence(st2, 1, n_decode=2)
     assert np.max(np.abs(rows2 - rows)) > 1e-3
     st3 = tiny_stack()
     st3["res_scale"][-1] = np.zeros_like(st3["res_scale"][-1])
     st4 = tiny_stack()
     st4["res_scale"][-1] = np.zeros_like(st4["res_scale"][-1])
     st4["conv_w"][-1] = st2["conv_w"][-1]
-    _, _, r3 = O.serving_stack_sequence(st3, 1, n_decode=2, chunk=4)
-    _, _, r4 = O.serving_stack_sequence(st4, 1, n_decode=2, chunk=4)
+    _, _, r3 = O.serving_stack_sequence(st3, 1, n_decode=2)
+    _, _, r4 = O.serving_stack_sequence(st4, 1, n_decode=2)
     assert np.array_equal(r3, r4)
