@@ -267,6 +267,32 @@ size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv, i
   return prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
 }
 
+}  // extern "C"
+
+namespace gdn {
+gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride, const void* v,
+                                int64_t v_stride, const float* a, const float* b,
+                                const int32_t* cu_seqlens, int32_t N, int32_t T, const float* S,
+                                const void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                int32_t chunk, int32_t qk_l2norm, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
+  if (chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if (T == 0 || N == 0) {
+    *nothing_to_do = true;
+    return GDN_OK;
+  }
+  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
+                                       qk_l2norm);
+  if (rc != GDN_OK) return rc;
+  if (dk != dv) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+}  // namespace gdn
+
+extern "C" {
+
 static gdn_status_t prefill_impl(const void* q, const void* k, int64_t qk_stride,
                                  const void* v, int64_t v_stride, const float* a, const float* b,
                                  const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
@@ -274,14 +300,10 @@ static gdn_status_t prefill_impl(const void* q, const void* k, int64_t qk_stride
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
                                  int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
                                  void* stream, StateSlots slots) {
-  if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
-  if (chunk != 64) return GDN_ERR_UNSUPPORTED;
-  if (T == 0 || N == 0) return GDN_OK;
-  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
-  gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
-                                       qk_l2norm);
-  if (rc != GDN_OK) return rc;
-  if (dk != dv) return GDN_ERR_UNSUPPORTED;
+  bool nothing = false;
+  gdn_status_t rc = check_prefill_args(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
+                                       o, Hk, Hv, dk, dv, chunk, qk_l2norm, &nothing);
+  if (rc != GDN_OK || nothing) return rc;
   const size_t need = prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
   if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;

@@ -220,6 +220,15 @@ gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
 size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
                                int32_t chunk);
 
+// Host-side checks of gdn_delta_rule_prefill_chunked's arguments (everything
+// but the workspace). GDN_OK with *nothing_to_do set: zero tokens or zero
+// sequences, a valid call that enqueues nothing.
+gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride, const void* v,
+                                int64_t v_stride, const float* a, const float* b,
+                                const int32_t* cu_seqlens, int32_t N, int32_t T, const float* S,
+                                const void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
+                                int32_t chunk, int32_t qk_l2norm, bool* nothing_to_do);
+
 gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_stride,
                                   const void* v, int64_t v_stride, const float* a,
                                   const float* b, const int32_t* cu, int32_t N, int32_t T,

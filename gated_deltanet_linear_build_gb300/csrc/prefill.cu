@@ -290,6 +290,9 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   auto kp = static_cast<const __nv_bfloat16*>(k);
   auto vp = static_cast<const __nv_bfloat16*>(v);
 
+  // Word 2 of the workspace header: the state pass's status. This state pass
+  // has no device-side waits, so it always reports GDN_OK.
+  if (cudaMemsetAsync(count + 2, 0, sizeof(int32_t), st) != cudaSuccess) return check_launch();
   gdn_status_t rc = launch_build_chunks(cu, N, kChunk, desc, L.capacity, count, bstatus, st);
   if (rc != GDN_OK) return rc;
 

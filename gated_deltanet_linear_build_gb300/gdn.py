@@ -33,6 +33,7 @@ EXPORTED_SYMBOLS = (
     "gdn_delta_rule_prefill_workspace_size",
     "gdn_delta_rule_prefill_chunked",
     "gdn_delta_rule_prefill_chunked_noalloc",
+    "gdn_delta_rule_prefill_chunked_noalloc_status",
     "gdn_causal_conv1d_fwd_slots",
     "gdn_causal_conv1d_update_slots",
     "gdn_delta_rule_decode_slots",
@@ -75,6 +76,7 @@ _SIGNATURES = {
     "gdn_delta_rule_prefill_chunked_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P,
                                                               _I32, _I32, _P, _P, _P, _I32, _I32,
                                                               _I32, _I32, _I32, _I32, _P]),
+    "gdn_delta_rule_prefill_chunked_noalloc_status": (ctypes.c_int, [_P, _P]),
     "gdn_causal_conv1d_fwd_slots": (ctypes.c_int, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _I32,
                                                    _I32, _I32, _I32, _I32, _I32, _P, _P, _I32,
                                                    _P]),
@@ -239,6 +241,14 @@ def delta_rule_prefill_chunked_noalloc(q, k, v, a, b, cu_seqlens, S, has_initial
     _check(rc, "gdn_delta_rule_prefill_chunked_noalloc")
 
 
+def delta_rule_prefill_chunked_noalloc_status(status, *, stream=None):
+    """Copy the two device-side status words of the last allocation-free
+    prefill (descriptor builder, state pass) into ``status`` (int32 [2], on
+    the device or in host memory), on the stream."""
+    rc = _lib().gdn_delta_rule_prefill_chunked_noalloc_status(_ptr(status), _stream(stream))
+    _check(rc, "gdn_delta_rule_prefill_chunked_noalloc_status")
+
+
 # ----------------------------------------------------------------------------
 # State-slot variants: conv_state [num_slots, C, 3] and S [num_slots, Hv, dv, dk]
 # form a cache; sequence n of the batch uses slot state_indices[n] (device
@@ -309,8 +319,7 @@ def selftest_bounded_wait(device_status, *, max_cycles: int = 2_000_000, stream=
 
 def prefill_workspace_status(workspace):
     """(descriptor builder status, state pass status) from a prefill workspace
-    once the call has completed (words 1 and 2; the second is defined for
-    dk = dv = 128 only)."""
+    once the call has completed (words 1 and 2)."""
     w = workspace[:12].view(torch.int32).cpu()
     return int(w[1]), int(w[2])
 

@@ -251,11 +251,11 @@ GDN_API size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32
  *               chunk-descriptor builder's status (GDN_OK, or
  *               GDN_ERR_INVALID_ARG for malformed cu_seqlens, which then count
  *               as no chunks at all: state and outputs are left untouched);
- *               for dk = dv = 128, word 2 (byte offset 8)
- *               is the state pass's status (GDN_OK; GDN_ERR_INVALID_ARG when
- *               the chunks do not cover a sequence, whose state and outputs
- *               are then left untouched; GDN_ERR_TIMEOUT when a bounded
- *               device-side wait gave up).
+ *               word 2 (byte offset 8) is the state pass's status (GDN_OK;
+ *               for dk = dv = 128 also GDN_ERR_INVALID_ARG when the chunks do
+ *               not cover a sequence, whose state and outputs are then left
+ *               untouched, or GDN_ERR_TIMEOUT when a bounded device-side wait
+ *               gave up).
  */
 GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,
                                             const void* v, int64_t v_stride,
@@ -285,14 +285,28 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k
  * GDN_ERR_WORKSPACE before anything is enqueued (for example, 2 x 512 tokens
  * with 32 v-heads of width 128 fit; 2 x 1024 tokens do not).
  *
- * Set-up: the first call on a device (with that device current) looks up the
- * array's device address with cudaGetSymbolAddress and caches it; make that
- * first call before capturing a stream. The call never allocates: no
+ * Every argument check and the size limit run before any CUDA call, so a
+ * rejected call touches no CUDA state.
+ *
+ * Set-up: the array's device address belongs to the library's module as
+ * loaded into one CUDA context. The first call made in a context (the calling
+ * thread's current context; with none current, the current device's primary
+ * context, which the call then makes current as any runtime call does) looks
+ * the address up with cudaGetSymbolAddress and caches it under that context's
+ * unique id, so another context on the same device, or the primary context
+ * re-created after cudaDeviceReset, gets its own lookup. Make the first call in
+ * a context before capturing a stream in it. The call never allocates: no
  * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Device-side status: the regular call reports what only the GPU can see
+ * (malformed cu_seqlens, a bounded wait that gave up) in words 1 and 2 of its
+ * workspace. Here those words live in the library's array, which the caller
+ * cannot address; gdn_delta_rule_prefill_chunked_noalloc_status copies them
+ * out.
  *
  * Sharing: every call on a device uses the same array, and the array keeps
  * whatever the last call left in it (each call writes everything it reads
- * back, and clears its own status word). Two calls whose work overlaps on the
+ * back, and clears its own status words). Two calls whose work overlaps on the
  * GPU -- on different streams, or from different host threads -- race on the
  * array and corrupt each other's results: serialise them.
  */
@@ -301,6 +315,24 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
     const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
     int32_t chunk, int32_t qk_l2norm, void* stream);
+
+/*
+ * Status words of the last gdn_delta_rule_prefill_chunked_noalloc call in the
+ * current context: enqueues, on `stream`, a copy of the two int32 words that
+ * gdn_delta_rule_prefill_chunked documents as its workspace words 1 and 2 into
+ * status[0] (the chunk-descriptor builder's status: GDN_OK, or
+ * GDN_ERR_INVALID_ARG for malformed cu_seqlens) and status[1] (the state
+ * pass's status: GDN_OK, GDN_ERR_INVALID_ARG, or GDN_ERR_TIMEOUT). Read them
+ * once the copy has completed; enqueue it on the stream of the call it
+ * reports on, after that call.
+ *
+ *   status  int32 [2]: device memory, or host memory (pinned memory keeps the
+ *           copy asynchronous; pageable host memory makes this call wait for
+ *           the stream).
+ * NULL status is GDN_ERR_INVALID_ARG. Allocates nothing. Before any
+ * noalloc prefill in this context the words read as GDN_OK.
+ */
+GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_noalloc_status(int32_t* status, void* stream);
 
 /*
  * State-slot variants. Source: "RTX 5070 Ti: close Qwen3.5-4B TTFT, TPOT, and

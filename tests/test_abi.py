@@ -136,6 +136,27 @@ def test_prefill_validation(lib):
     assert prefill(lib, N=0) == OK
 
 
+def prefill_noalloc(lib, **kw):
+    args = dict(q=A16, k=A16, qk_stride=4096, v=A16, v_stride=4096, a=A16, b=A16, cu=A16, N=2,
+                T=512, S=A16, has=None, o=A16, Hk=16, Hv=32, dk=128, dv=128, chunk=64, l2=0)
+    args.update(kw)
+    return lib.gdn_delta_rule_prefill_chunked_noalloc(*args.values(), None)
+
+
+def test_prefill_noalloc_validation_before_any_cuda_call(lib):
+    # Every check of the regular entry point, and the fixed array's size limit,
+    # run before the call looks up its scratch (no CUDA call on these paths).
+    assert prefill_noalloc(lib, cu=None) == INVALID
+    assert prefill_noalloc(lib, q=None) == INVALID
+    assert prefill_noalloc(lib, chunk=32) == UNSUPPORTED
+    assert prefill_noalloc(lib, dk=64) == UNSUPPORTED
+    assert prefill_noalloc(lib, Hv=24) == INVALID                # Hv % Hk != 0
+    assert prefill_noalloc(lib, S=A8) == ALIGN
+    assert prefill_noalloc(lib, T=2048) == WORKSPACE             # beyond the 64 MiB array
+    assert prefill_noalloc(lib, T=0) == OK
+    assert lib.gdn_delta_rule_prefill_chunked_noalloc_status(None, None) == INVALID
+
+
 def test_decode_step_fused_validation(lib):
     f = lib.gdn_decode_step_fused
     C = 2 * 16 * 128 + 32 * 128

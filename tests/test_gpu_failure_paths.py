@@ -64,8 +64,9 @@ def test_malformed_cu_seqlens_reported_on_device(G, d):
     torch.cuda.synchronize()
     builder, state_pass = G.prefill_workspace_status(ws)
     assert builder == G.GDN_ERR_INVALID_ARG
-    if d == 128:
-        assert state_pass == G.GDN_ERR_INVALID_ARG
+    # the tensor-core state pass sees the missing chunks; the SIMT one (d < 128)
+    # has no waits and reports GDN_OK
+    assert state_pass == (G.GDN_ERR_INVALID_ARG if d == 128 else G.GDN_OK)
     # no chunk records exist, so the state pass touched neither S nor o
     assert torch.equal(S, dev(S0))
     assert bool((o.float() == SENTINEL).all())

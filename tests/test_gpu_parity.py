@@ -1,9 +1,11 @@
 """Parity of the CUDA path (through the C ABI) against the CPU oracle.
 
-Tolerances (relative error = max|x - ref| / max|ref| over the tensor):
+Tolerances (``parity.py``; relative error = max|x - ref| / max|ref|):
   * descriptors and conv_state bytes: bit-exact;
-  * BF16 outputs (conv y, delta o): 2e-2;
-  * float32 recurrent state S: 1e-4.
+  * conv outputs y: elementwise, one BF16 rounding of a float32 value;
+  * delta-rule outputs o: 2e-2 over the tensor, over each v-head and over each
+    (token, v-head) row;
+  * float32 recurrent state S: 1e-4 over each (sequence, v-head) state.
 Exact-chunk and whole-sequence conv dispatch must be byte-identical, and so must
 a prefill split across steps against one longer prefill (same kernels, same
 arithmetic per element).
@@ -16,11 +18,9 @@ from oracle import gdn_oracle as O
 from gated_deltanet_linear_build_gb300 import synth
 
 from devutil import bf16_dev, bf16_host_bits, bf16_values, dev
+from parity import assert_S, assert_conv_y, assert_o
 
 pytestmark = pytest.mark.gpu
-
-TOL_BF16 = 2e-2
-TOL_STATE = 1e-4
 
 
 @pytest.fixture(scope="module")
@@ -113,9 +113,8 @@ def conv_gpu(G, case, mode="chunks", silu=True, x_stride_pad=0):
 def check_conv(case, y, st, silu=True):
     yr, sr = O.causal_conv1d_fwd(case["x"], case["w"], case["bias"], case["conv_state"],
                                  case["has_initial_state"], case["cu_seqlens"], apply_silu=silu)
-    assert O.rel_err(bf16_values(y), yr) < TOL_BF16
     # Elementwise: one BF16 rounding of an fp32 value (plus fp32 rounding).
-    assert np.all(np.abs(bf16_values(y) - yr) <= 2.0 ** -8 * np.abs(yr) + 1e-6)
+    assert_conv_y(bf16_values(y), yr)
     assert np.array_equal(bf16_host_bits(st), O.to_bf16(sr))
 
 
@@ -158,7 +157,7 @@ def test_conv_update_full_size(G):
     G.causal_conv1d_update(x, w, b, st, y)
     torch.cuda.synchronize()
     yr, sr = O.causal_conv1d_update(conv["x"], conv["w"], conv["bias"], conv["conv_state"])
-    assert O.rel_err(bf16_values(y), yr) < TOL_BF16
+    assert_conv_y(bf16_values(y), yr)
     assert np.array_equal(bf16_host_bits(st), O.to_bf16(sr))
 
 
@@ -222,10 +221,8 @@ def check_decode(d, o, S, qk_l2norm=False):
     Hv, dv, dk = d["v"].shape[1], d["v"].shape[2], d["q"].shape[2]
     orf, Sr = O.delta_rule_decode(d["q"], d["k"], d["v"], d["a"], d["b"],
                                   d["S0"].reshape(N, Hv, dv, dk), qk_l2norm=qk_l2norm)
-    eo = O.rel_err(bf16_values(o), orf)
-    es = O.rel_err(S.cpu().numpy(), Sr)
-    assert eo < TOL_BF16, eo
-    assert es < TOL_STATE, es
+    eo = assert_o(bf16_values(o), orf)
+    es = assert_S(S.cpu().numpy(), Sr)
     return eo, es
 
 
@@ -277,9 +274,8 @@ def check_prefill(d, o, S, qk_l2norm=False, heads=None):
     og, Sg = bf16_values(o), S.cpu().numpy().astype(np.float64)
     if heads is not None:
         og, orf, Sg, Sr = og[:, heads], orf[:, heads], Sg[:, heads], Sr[:, heads]
-    eo, es = O.rel_err(og, orf), O.rel_err(Sg, Sr)
-    assert eo < TOL_BF16, eo
-    assert es < TOL_STATE, es
+    eo = assert_o(og, orf)
+    es = assert_S(Sg, Sr)
     return eo, es
 
 
@@ -305,9 +301,10 @@ def test_prefill_l2norm_flag(G):
 
 
 def test_prefill_full_size(G):
+    # 2 x 1024 tokens, all 32 v-heads of both sequences against the oracle.
     d = synth.prefill(3)
     o, S = prefill_gpu(G, d)
-    check_prefill(d, o, S, heads=[0, 1, 2, 15, 16, 30, 31])
+    check_prefill(d, o, S)
 
 
 def test_prefill_then_decode_equals_longer_prefill(G):
@@ -325,8 +322,8 @@ def test_prefill_then_decode_equals_longer_prefill(G):
         step["S0"] = S.cpu().numpy()
         o_t, S = decode_gpu(G, step)
         ref = bf16_values(o_full)[rows]
-        assert O.rel_err(bf16_values(o_t), ref) < TOL_BF16
-    assert O.rel_err(S.cpu().numpy(), S_full.cpu().numpy()) < TOL_STATE
+        assert_o(bf16_values(o_t), ref)
+    assert_S(S.cpu().numpy(), S_full.cpu().numpy())
 
 
 def test_prefill_slow_decay_state_precision(G):
@@ -337,19 +334,4 @@ def test_prefill_slow_decay_state_precision(G):
     z = rng.standard_normal(d["a"].shape) - 4.5
     d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
     o, S = prefill_gpu(G, d)
-    check_prefill(d, o, S, heads=[0, 9, 31])
-
-
-def test_prefill_full_size_all_heads_one_sequence(G):
-    d = synth.prefill(3)
-    o, S = prefill_gpu(G, d)
-    one = {k: d[k] for k in d}
-    for key in ("q", "k", "v", "a", "b"):
-        one[key] = d[key][:1024]
-    one["cu_seqlens"] = d["cu_seqlens"][:2]
-    one["S0"] = d["S0"][:1]
-    one["has_initial_state"] = d["has_initial_state"][:1]
-    orf, Sr = O.delta_rule_prefill(one["q"], one["k"], one["v"], one["a"], one["b"],
-                                   one["cu_seqlens"], one["S0"], one["has_initial_state"])
-    assert O.rel_err(bf16_values(o)[:1024], orf) < TOL_BF16
-    assert O.rel_err(S.cpu().numpy()[:1], Sr) < TOL_STATE
+    check_prefill(d, o, S)

@@ -7,6 +7,9 @@ that cache plus a per-sequence slot map. Checked here, for every kernel of the
 path (conv prefill with exact chunks and whole-sequence dispatch, conv update,
 decode with d = 128 and d = 64, chunked prefill with d = 128 and d = 64):
 
+  * a valid entry matches the oracle run on the states gathered from the
+    cache (conv outputs elementwise and conv state bytes exactly; delta-rule
+    outputs and states within the BF16 / float32 bars);
   * a valid entry gives bit-identical outputs and new state to the call
     without the suffix on the gathered states (the same arithmetic runs);
   * slots that no sequence names keep their bytes;
@@ -17,9 +20,11 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import gdn_oracle as O
 from gated_deltanet_linear_build_gb300 import synth
 
-from devutil import bf16_dev, dev
+from devutil import bf16_dev, bf16_host_bits, bf16_values, dev
+from parity import assert_S, assert_conv_y, assert_o
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +63,19 @@ def gather(cache, idx):
         if 0 <= s < cache.shape[0]:
             out[n] = cache[s]
     return out
+
+
+def gather_np(cache, idx):
+    """Host copy of the batch's states from the host cache (zeros for padding)."""
+    out = np.zeros((len(idx),) + cache.shape[1:], dtype=cache.dtype)
+    for n, s in enumerate(idx):
+        if 0 <= s < cache.shape[0]:
+            out[n] = cache[s]
+    return out
+
+
+def valid_entries(idx, num_slots):
+    return [n for n, s in enumerate(idx) if 0 <= s < num_slots]
 
 
 def check_cache(cache_after, cache_before, dense_after, idx):
@@ -100,7 +118,8 @@ def test_conv_fwd_slots(G, chunked):
     T, N = case["x"].shape[0], len(lens)
     idx = slot_map(82, N, num_slots, pads=[2, 4])
     rng = np.random.default_rng(83)
-    cache0 = bf16_dev(synth.normal_bf16(rng, (num_slots, C, 3)))
+    cache_h = synth.normal_bf16(rng, (num_slots, C, 3))
+    cache0 = bf16_dev(cache_h)
     x, w, bias = bf16_dev(case["x"]), bf16_dev(case["w"]), bf16_dev(case["bias"])
     cu, has = dev(cu_h), dev(case["has_initial_state"])
     chunks = num = None
@@ -122,6 +141,13 @@ def test_conv_fwd_slots(G, chunked):
     assert same_bits(y[vr], y_d[vr])
     assert bool((y[pr].float() == SENTINEL).all())
     check_cache(cache, cache0, dense, idx)
+    # the oracle on the gathered states
+    yr, sr = O.causal_conv1d_fwd(case["x"], case["w"], case["bias"], gather_np(cache_h, idx),
+                                 case["has_initial_state"], cu_h)
+    vr_h = vr.cpu().numpy()
+    assert_conv_y(bf16_values(y)[vr_h], yr[vr_h])
+    for n in valid_entries(idx, num_slots):
+        assert np.array_equal(bf16_host_bits(cache[int(idx[n])]), O.to_bf16(sr[n])), n
 
 
 def test_conv_update_slots(G):
@@ -129,7 +155,8 @@ def test_conv_update_slots(G):
     case = synth.conv_update_case(84, N, C, bias=True)
     idx = slot_map(85, N, num_slots, pads=[0, 5])
     rng = np.random.default_rng(86)
-    cache0 = bf16_dev(synth.normal_bf16(rng, (num_slots, C, 3)))
+    cache_h = synth.normal_bf16(rng, (num_slots, C, 3))
+    cache0 = bf16_dev(cache_h)
     x, w, bias = bf16_dev(case["x"]), bf16_dev(case["w"]), bf16_dev(case["bias"])
     dense = gather(cache0, idx)
     y_d = torch.empty((N, C), dtype=torch.bfloat16, device="cuda")
@@ -142,6 +169,11 @@ def test_conv_update_slots(G):
     assert same_bits(y[vr], y_d[vr])
     assert bool((y[pr].float() == SENTINEL).all())
     check_cache(cache, cache0, dense, idx)
+    yr, sr = O.causal_conv1d_update(case["x"], case["w"], case["bias"], gather_np(cache_h, idx))
+    ok = valid_entries(idx, num_slots)
+    assert_conv_y(bf16_values(y)[ok], yr[ok])
+    for n in ok:
+        assert np.array_equal(bf16_host_bits(cache[int(idx[n])]), O.to_bf16(sr[n])), n
 
 
 @pytest.mark.parametrize("d,hk,hv", [(128, 4, 8), (64, 2, 4)])
@@ -150,7 +182,8 @@ def test_decode_slots(G, d, hk, hv):
     case = synth.delta_case(87 + d, [1] * N, hk, hv, d, d, normed_qk=False)
     idx = slot_map(88, N, num_slots, pads=[3, 9])
     rng = np.random.default_rng(89)
-    cache0 = dev((0.02 * rng.standard_normal((num_slots, hv, d, d))).astype(np.float32))
+    cache_h = (0.02 * rng.standard_normal((num_slots, hv, d, d))).astype(np.float32)
+    cache0 = dev(cache_h)
     q, k, v = bf16_dev(case["q"]), bf16_dev(case["k"]), bf16_dev(case["v"])
     a, b = dev(case["a"]), dev(case["b"])
     dense = gather(cache0, idx)
@@ -164,6 +197,11 @@ def test_decode_slots(G, d, hk, hv):
     assert same_bits(o[vr], o_d[vr])
     assert bool((o[pr].float() == SENTINEL).all())
     check_cache(cache, cache0, dense, idx)
+    o_r, S_r = O.delta_rule_decode(case["q"], case["k"], case["v"], case["a"], case["b"],
+                                   gather_np(cache_h, idx), qk_l2norm=True)
+    ok = valid_entries(idx, num_slots)
+    assert_o(bf16_values(o)[ok], o_r[ok])
+    assert_S(np.stack([cache[int(idx[n])].cpu().numpy() for n in ok]), S_r[ok])
 
 
 @pytest.mark.parametrize("d,hk,hv", [(128, 4, 8), (64, 2, 4)])
@@ -177,7 +215,8 @@ def test_prefill_slots(G, d, hk, hv):
     T = int(cu_h[-1])
     idx = slot_map(91, N, num_slots, pads=[3])
     rng = np.random.default_rng(92)
-    cache0 = dev((0.05 * rng.standard_normal((num_slots, hv, d, d))).astype(np.float32))
+    cache_h = (0.05 * rng.standard_normal((num_slots, hv, d, d))).astype(np.float32)
+    cache0 = dev(cache_h)
     q, k, v = bf16_dev(case["q"]), bf16_dev(case["k"]), bf16_dev(case["v"])
     a, b = dev(case["a"]), dev(case["b"])
     cu, has = dev(cu_h), dev(case["has_initial_state"])
@@ -194,6 +233,12 @@ def test_prefill_slots(G, d, hk, hv):
     assert same_bits(o[vr], o_d[vr])
     assert bool((o[pr].float() == SENTINEL).all())
     check_cache(cache, cache0, dense, idx)
+    o_r, S_r = O.delta_rule_prefill(case["q"], case["k"], case["v"], case["a"], case["b"], cu_h,
+                                    gather_np(cache_h, idx), case["has_initial_state"])
+    vr_h = vr.cpu().numpy()
+    ok = valid_entries(idx, num_slots)
+    assert_o(bf16_values(o)[vr_h], o_r[vr_h])
+    assert_S(np.stack([cache[int(idx[n])].cpu().numpy() for n in ok]), S_r[ok])
 
 
 def test_all_padding_touches_nothing(G):

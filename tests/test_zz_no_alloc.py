@@ -11,7 +11,13 @@ its own in a fresh process.
 Two calls in a row, with different inputs and shapes, must each match the
 regular entry point (which gets its own workspace) within the tolerances of
 the parity tests: the array keeps the first call's contents, and the second
-call must not be affected by them.
+call must not be affected by them. (The regular entry point is itself checked
+against the oracle by the parity tests; this variant only changes where the
+scratch lives, so it is compared with the regular call.) The device-side
+status words, which live in the library's array, are read back through
+gdn_delta_rule_prefill_chunked_noalloc_status: GDN_OK after a good call,
+GDN_ERR_INVALID_ARG after one with malformed cu_seqlens (which then leaves
+state and outputs untouched).
 """
 import numpy as np
 import pytest
@@ -82,3 +88,34 @@ def test_noalloc_small_head_dim_and_size_limit(G):
     with pytest.raises(G.GdnError) as exc:
         run_both(G, big)
     assert exc.value.status == G.GDN_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_noalloc_status_words(G, d):
+    hk, hv, T = 2, 4, 100
+    case = synth.delta_case(75, [T], hk, hv, d, d, s0_std=0.05)
+    status = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    # a good call: both words GDN_OK
+    q, k, v = bf16_dev(case["q"]), bf16_dev(case["k"]), bf16_dev(case["v"])
+    a, b = dev(case["a"]), dev(case["b"])
+    S = dev(case["S0"])
+    o = torch.empty((T, hv, d), dtype=torch.bfloat16, device="cuda")
+    G.delta_rule_prefill_chunked_noalloc(q, k, v, a, b, dev(case["cu_seqlens"]), S,
+                                         dev(case["has_initial_state"]), o)
+    G.delta_rule_prefill_chunked_noalloc_status(status)
+    torch.cuda.synchronize()
+    assert status.tolist() == [G.GDN_OK, G.GDN_OK]
+    # malformed cu_seqlens (the second entry decreases): reported, nothing touched
+    N = 2
+    S0 = (0.05 * np.random.default_rng(76).standard_normal((N, hv, d, d))).astype(np.float32)
+    S = dev(S0)
+    o = torch.full((T, hv, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    G.delta_rule_prefill_chunked_noalloc(q, k, v, a, b, dev(np.array([0, T, 50], np.int32)), S,
+                                         dev(np.ones(N, np.uint8)), o)
+    host = torch.full((2,), -7, dtype=torch.int32).pin_memory()
+    G.delta_rule_prefill_chunked_noalloc_status(host)
+    torch.cuda.synchronize()
+    assert host[0].item() == G.GDN_ERR_INVALID_ARG
+    assert host[1].item() == (G.GDN_ERR_INVALID_ARG if d == 128 else G.GDN_OK)
+    assert torch.equal(S, dev(S0))
+    assert bool((o.float() == 3.0).all())
