@@ -8,9 +8,10 @@ prefill steps of at most 2048 tokens, then 128 decode steps over all 32
 sequences. Every prefill step builds its exact 8-token conv descriptors once
 and reuses them in all 24 layers; each layer runs the conv (prefill or update)
 and the delta rule (chunked prefill or decode) on q/k/v read in place from the
-conv output, q/k L2-normalised in the kernel. Inputs are synthetic (seeded
-normal x, gates a = exp(-softplus(z)), b = sigmoid(z)) and distinct for every
-layer and step (about 11 GB per sweep, far larger than L2).
+conv output, q/k L2-normalised and the gates activated from their logits
+(a = exp(-softplus(z_a)), b = sigmoid(z_b)) in the kernel. Inputs are synthetic
+(seeded normal x and gate logits) and distinct for every layer and step (about
+11 GB per sweep, far larger than L2).
 
 The sweep is captured once as a CUDA graph and replayed; `value` is tokens
 through the 24-layer stack per second with inputs resident in HBM. `e2e` runs
@@ -258,10 +259,10 @@ class Workload:
         bf16 = torch.bfloat16
 
         def gates(T):
-            z1 = torch.randn((T, HV), generator=g, device=device)
-            z2 = torch.randn((T, HV), generator=g, device=device)
-            return (torch.exp(-torch.nn.functional.softplus(z1)).contiguous(),
-                    torch.sigmoid(z2).contiguous())
+            # raw gate logits z_a, z_b ~ N(0, 1): the delta-rule kernels compute
+            # a = exp(-softplus(z_a)) and b = sigmoid(z_b) themselves
+            return (torch.randn((T, HV), generator=g, device=device).contiguous(),
+                    torch.randn((T, HV), generator=g, device=device).contiguous())
 
         self.px = [[torch.randn((m[4], C), generator=g, device=device, dtype=bf16)
                     for _ in range(LAYERS)] for m in self.meta]
@@ -728,8 +729,8 @@ def run_case(args):
         return torch.randn(shape, generator=g, device=dev, dtype=dtype)
 
     def gates(T):
-        return (torch.exp(-torch.nn.functional.softplus(randn(T, HV))).contiguous(),
-                torch.sigmoid(randn(T, HV)).contiguous())
+        # raw gate logits; the kernels activate them (GDN_FLAG_GATE_LOGITS)
+        return randn(T, HV).contiguous(), randn(T, HV).contiguous()
 
     case = args.case
     if case == "conv_prefill":
@@ -773,7 +774,7 @@ def run_case(args):
             q = y[:, :HK * D].view(N_SEQS, HK, D)
             k = y[:, HK * D:2 * HK * D].view(N_SEQS, HK, D)
             v = y[:, 2 * HK * D:].view(N_SEQS, HV, D)
-            gdn.delta_rule_decode(q, k, v, a, b, S, o, qk_l2norm=True)
+            gdn.delta_rule_decode(q, k, v, a, b, S, o, qk_l2norm=True, gate_logits=True)
         work, unit, bound = per, "GB/s", "hbm"
     else:  # prefill: 2 x 1024 tokens, 32 v-heads over 16 k-heads, d = 128
         T, n = 2048, 2
@@ -793,7 +794,8 @@ def run_case(args):
             q = y[:, :HK * D].view(T, HK, D)
             k = y[:, HK * D:2 * HK * D].view(T, HK, D)
             v = y[:, 2 * HK * D:].view(T, HV, D)
-            gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu, S, has, o, ws, qk_l2norm=True)
+            gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu, S, has, o, ws, qk_l2norm=True,
+                                           gate_logits=True)
         work, unit, bound = prefill_flops([64] * 32), "TFLOP/s", "tensor"
 
     stream = torch.cuda.Stream(device=dev)

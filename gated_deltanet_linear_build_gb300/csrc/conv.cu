@@ -374,6 +374,7 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
             if (it % kCvGroups != pw) continue;
             const int st = cv_slot(it), rd = cv_round(it);
             if (rd > 0 && !mbar_wait_sleep(empty + st, (rd - 1) & 1, 128)) {
+              record_device_status(GDN_ERR_TIMEOUT);   // the compute group stopped
               ok = false;
               break;
             }
@@ -432,6 +433,8 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
         CvMeta m;
         m.rows = -1;
         post(m, 0, st);
+      } else {
+        record_device_status(GDN_ERR_TIMEOUT);
       }
     }
     return;
@@ -469,8 +472,12 @@ conv_fwd_stream_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
   }
   for (int it = g;; it += kCvGroups) {
     const int st = cv_slot(it);
-    // A wait that gives up (the producer stopped) ends the stream.
-    if (!mbar_wait_sleep(full + st, cv_round(it) & 1)) break;
+    // A wait that gives up (the producer stopped) ends the stream; only stages
+    // whose copies have all landed are ever computed and stored.
+    if (!mbar_wait_sleep(full + st, cv_round(it) & 1)) {
+      record_device_status(GDN_ERR_TIMEOUT);
+      break;
+    }
     const CvMeta m = meta[st];
     if (m.rows < 0) break;
     const unsigned char* stage = sm + st * kCvStageBytes;
@@ -646,5 +653,7 @@ gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
       static_cast<__nv_bfloat16*>(conv_state), (int)C, (int)silu,
       static_cast<__nv_bfloat16*>(y), slots));
 }
+
+GDN_DEFINE_STATUS_GATHER(gather_status_conv)
 
 }  // namespace gdn

@@ -55,7 +55,7 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
                     int64_t qk_stride, const __nv_bfloat16* __restrict__ v, int64_t v_stride,
                     const float* __restrict__ a, const float* __restrict__ b,
                     float* __restrict__ S, __nv_bfloat16* __restrict__ o, int Hk, int Hv,
-                    int qk_l2norm, const StateSlots slots) {
+                    int flags, const StateSlots slots) {
   using Cfg = DecodeCfg<DK, DV>;
   constexpr int LPR = Cfg::kLanesPerRow;
   __shared__ float s_o[DV];
@@ -73,7 +73,7 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
 
   float4 k4 = ld_bf16x4(k + n * qk_stride + (int64_t)g * DK + sub * 4);
   float4 q4 = ld_bf16x4(q + n * qk_stride + (int64_t)g * DK + sub * 4);
-  if (qk_l2norm) {
+  if (flags & kFlagL2) {
     const float kk = group_sum<LPR>(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
     const float qq = group_sum<LPR>(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
     const float rk = 1.0f / sqrtf(kk + 1e-6f), rq = 1.0f / sqrtf(qq + 1e-6f);
@@ -81,7 +81,8 @@ delta_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __
     q4 = make_float4(q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq);
   }
   const float kq = group_sum<LPR>(k4.x * q4.x + k4.y * q4.y + k4.z * q4.z + k4.w * q4.w);
-  const float av = __ldg(a + nh), bv = __ldg(b + nh);
+  const bool gl = (flags & kFlagGateLogits) != 0;
+  const float av = gate_decay(__ldg(a + nh), gl), bv = gate_write(__ldg(b + nh), gl);
 
   float* Sh = S + ((size_t)slot * Hv + h) * DV * DK;
   const __nv_bfloat16* vh = v + n * v_stride + (int64_t)h * DV;
@@ -160,7 +161,8 @@ struct DecStage {
   static constexpr int kConvOff = kDecStages * kDecStageBytes;            // fused: conv ring
   static constexpr int kYOff = kConvOff + (kFused ? kFSlots * kFSlot : 0);  // fused: y ring
   static constexpr int kBarOff = kYOff + (kFused ? kFYSlots * kFYSlot : 0);
-  static constexpr int kSmem = kBarOff + 2 * (kDecStages + kFSlots + kFYSlots) * 8 + 64;
+  static constexpr int kAbortOff = kBarOff + 2 * (kDecStages + kFSlots + kFYSlots) * 8;
+  static constexpr int kSmem = kAbortOff + 64;
   // compute warps, state producer, [conv-input producer, conv warps]
   static constexpr int kProdWarp = kDecWarps;
   static constexpr int kConvWarp0 = kDecWarps + 2;
@@ -182,7 +184,7 @@ struct DecodeArgs {
   const float *a, *b;
   float* S;
   __nv_bfloat16* o;
-  int Hk, Hv, qk_l2norm, units;
+  int Hk, Hv, flags, units;   // flags: GDN_FLAG_* bits
   StateSlots slots;   // unfused only: sequence -> state slot
 };
 
@@ -226,11 +228,16 @@ delta_decode_stream_kernel(const DecodeArgs p) {
   uint64_t* cempty = cfull + kFSlots;
   uint64_t* yfull = cempty + kFSlots;      // fused: conv-output ring
   uint64_t* yempty = yfull + kFYSlots;
+  // Set by the first role whose bounded wait gives up; every other wait then
+  // gives up at once, no role stores a unit it has not finished, and the
+  // state producer drains its copies in flight before the CTA exits.
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + Cfg::kAbortOff);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
   const int Hv = p.Hv, ratio = p.Hv / p.Hk;
   const int my_units = (p.units - (int)blockIdx.x + G - 1) / G;   // units blockIdx.x + i G
   if (tid == 0) {
+    *abort = 0;
     for (int st = 0; st < kDecStages; ++st) {
       mbar_init(full + st, 1);
       mbar_init(empty + st, kDecWarps);
@@ -279,7 +286,7 @@ delta_decode_stream_kernel(const DecodeArgs p) {
       // behind the state rows.
       for (int i = 0; i < my_units; ++i) {
         const int cs = i % kFSlots;
-        const bool ok = i < kFSlots || mbar_wait(cempty + cs, ((i / kFSlots) - 1) & 1);
+        const bool ok = i < kFSlots || mbar_wait_abortable(cempty + cs, ((i / kFSlots) - 1) & 1, abort);
         if (!__all_sync(0xffffffffu, ok)) break;
         int n, h, g, part;
         unit_coords(blockIdx.x + i * G, n, h, g, part);
@@ -325,7 +332,7 @@ delta_decode_stream_kernel(const DecodeArgs p) {
         // taps 0-3 and bias of global channel cg (issued before the wait)
         const uint2 wu = __ldg(reinterpret_cast<const uint2*>(p.w) + cg);
         const float bias = p.bias ? __bfloat162float(p.bias[cg]) : 0.f;
-        if (!mbar_wait_sleep(cfull + cs, (i / kFSlots) & 1, 64)) break;
+        if (!mbar_wait_abortable(cfull + cs, (i / kFSlots) & 1, abort, 64)) break;
         const unsigned char* cslot = sm + Cfg::kConvOff + cs * kFSlot;
         const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(cslot + offx);
         const __nv_bfloat16* ss = reinterpret_cast<const __nv_bfloat16*>(cslot + offs);
@@ -348,7 +355,8 @@ delta_decode_stream_kernel(const DecodeArgs p) {
           d[2] = xbf;
         }
         // The y slot is free once the compute warps have read its previous unit.
-        if (i >= kFYSlots && !mbar_wait_sleep(yempty + ys, ((i / kFYSlots) - 1) & 1, 64)) break;
+        if (i >= kFYSlots && !mbar_wait_abortable(yempty + ys, ((i / kFYSlots) - 1) & 1, abort, 64))
+          break;
         reinterpret_cast<__nv_bfloat16*>(sm + Cfg::kYOff + ys * kFYSlot + offy)[c] = y;
         __syncwarp();
         if (lane == 0)
@@ -384,10 +392,14 @@ delta_decode_stream_kernel(const DecodeArgs p) {
                    2 * kDecRows, full + st);
         }
       };
-      for (int i = 0; i < my_units && i < kDecStages; ++i) issue_load(i);
-      for (int i = 0; i < my_units; ++i) {
+      int issued = 0;   // units whose loads have been issued: [0, issued)
+      for (; issued < my_units && issued < kDecStages; ++issued) issue_load(issued);
+      int i = 0;
+      for (; i < my_units; ++i) {
         const int st = i % kDecStages;
-        mbar_wait(empty + st, (i / kDecStages) & 1);
+        // The compute warps stopped (or another role gave up): store nothing
+        // more, the unit's rows are not all updated.
+        if (!mbar_wait_abortable(empty + st, (i / kDecStages) & 1, abort)) break;
         const int unit = blockIdx.x + i * G;
         int n, h, g, part;
         unit_coords(unit, n, h, g, part);
@@ -403,15 +415,24 @@ delta_decode_stream_kernel(const DecodeArgs p) {
         if (i >= 1 && i - 1 + kDecStages < my_units) {
           asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
           issue_load(i - 1 + kDecStages);
+          issued = i + kDecStages;
         }
       }
       bulk_wait_all();
+      // After an abort, units [i, issued) may still have loads landing in
+      // their stages (distinct stages: fewer than kDecStages of them); their
+      // phases are the latest armed ones, so waiting for them is exact.
+      // Bounded, not abortable: no copy may be in flight when the CTA exits.
+      for (int j = i; j < issued; ++j)
+        if (!mbar_wait(full + j % kDecStages, (j / kDecStages) & 1))
+          record_device_status(GDN_ERR_TIMEOUT);
     }
     return;
   }
 
   // Compute warps: rows 4 warp .. 4 warp + 3 of every unit; lane l holds
   // columns 4 l .. 4 l + 3.
+  const bool gl = (p.flags & kFlagGateLogits) != 0;
   float a_nxt = 0.f, b_nxt = 0.f;
   if (my_units > 0) {
     a_nxt = __ldg(p.a + blockIdx.x / kDecUnitsPerHead);
@@ -420,20 +441,21 @@ delta_decode_stream_kernel(const DecodeArgs p) {
   for (int i = 0; i < my_units; ++i) {
     const int st = i % kDecStages;
     const int unit = blockIdx.x + i * G;
-    const float av = a_nxt, bv = b_nxt;
+    const float av = gate_decay(a_nxt, gl), bv = gate_write(b_nxt, gl);
     if (i + 1 < my_units) {
       a_nxt = __ldg(p.a + (unit + G) / kDecUnitsPerHead);
       b_nxt = __ldg(p.b + (unit + G) / kDecUnitsPerHead);
     }
     // Waiting warps back off, so they take no issue slots from the producer
-    // warps on their sub-partition.
-    mbar_wait_sleep(full + st, (i / kDecStages) & 1, 32);
+    // warps on their sub-partition. A wait that gives up stops this warp: it
+    // no longer arrives on "empty", so the producer stores nothing more.
+    if (!mbar_wait_abortable(full + st, (i / kDecStages) & 1, abort, 32)) break;
     unsigned char* stage = sm + st * kDecStageBytes;
     uint2 ku, qu, vu;
     if constexpr (kFused) {
       // k, q, v from the conv warps' ring (BF16, as the unfused stage holds them)
       const int ys = i % kFYSlots;
-      mbar_wait_sleep(yfull + ys, (i / kFYSlots) & 1, 32);
+      if (!mbar_wait_abortable(yfull + ys, (i / kFYSlots) & 1, abort, 32)) break;
       const unsigned char* yslot = sm + Cfg::kYOff + ys * kFYSlot;
       ku = reinterpret_cast<const uint2*>(yslot)[lane];
       qu = reinterpret_cast<const uint2*>(yslot + 256)[lane];
@@ -476,7 +498,7 @@ delta_decode_stream_kernel(const DecodeArgs p) {
       sq[j] = __shfl_sync(0xffffffffu, red, 16 + 4 * j);
     }
     float rk = 1.f, rq = 1.f;
-    if (p.qk_l2norm) {
+    if (p.flags & kFlagL2) {
       rk = 1.0f / sqrtf(kk + 1e-6f);
       rq = 1.0f / sqrtf(qq + 1e-6f);
     }
@@ -513,14 +535,14 @@ delta_decode_stream_kernel(const DecodeArgs p) {
 template <int DK, int DV>
 gdn_status_t launch_decode_t(const void* q, const void* k, int64_t qk_stride, const void* v,
                              int64_t v_stride, const float* a, const float* b, float* S,
-                             void* o, int N, int Hk, int Hv, int qk_l2norm, cudaStream_t st,
+                             void* o, int N, int Hk, int Hv, int flags, cudaStream_t st,
                              StateSlots slots) {
   using Cfg = DecodeCfg<DK, DV>;
   return check_launch(launch_pdl(
       delta_decode_kernel<DK, DV>, dim3(N * Hv), dim3(Cfg::kThreads), 0, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride,
       static_cast<const __nv_bfloat16*>(v), v_stride, a, b, S, static_cast<__nv_bfloat16*>(o),
-      Hk, Hv, qk_l2norm, slots));
+      Hk, Hv, flags, slots));
 }
 
 template <int DK>
@@ -564,7 +586,7 @@ gdn_status_t launch_decode_stream(const DecodeArgs& p, cudaStream_t st) {
 gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
                                  const void* bias, const void* st_in, void* st_out,
                                  const float* a, const float* b, float* S, void* o, int32_t N,
-                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t qk_l2norm,
+                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t flags,
                                  cudaStream_t st) {
   DecodeArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -581,7 +603,7 @@ gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
   p.o = static_cast<__nv_bfloat16*>(o);
   p.Hk = Hk;
   p.Hv = Hv;
-  p.qk_l2norm = qk_l2norm;
+  p.flags = flags;
   p.units = N * Hv * kDecUnitsPerHead;
   return launch_decode_stream<true>(p, st);
 }
@@ -589,7 +611,7 @@ gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
 gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride,
                                  const void* v, int64_t v_stride, const float* a,
                                  const float* b, float* S, void* o, int32_t N, int32_t Hk,
-                                 int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
+                                 int32_t Hv, int32_t dk, int32_t dv, int32_t flags,
                                  cudaStream_t st, StateSlots slots) {
   if (dk == 128 && dv == 128) {
     DecodeArgs p{};
@@ -604,18 +626,20 @@ gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride
     p.o = static_cast<__nv_bfloat16*>(o);
     p.Hk = Hk;
     p.Hv = Hv;
-    p.qk_l2norm = qk_l2norm;
+    p.flags = flags;
     p.units = N * Hv * kDecUnitsPerHead;
     p.slots = slots;
     return launch_decode_stream<false>(p, st);
   }
   switch (dk) {
-    case 16: return launch_decode_dv<16>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
-    case 32: return launch_decode_dv<32>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
-    case 64: return launch_decode_dv<64>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
-    case 128: return launch_decode_dv<128>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, qk_l2norm, st, slots);
+    case 16: return launch_decode_dv<16>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, flags, st, slots);
+    case 32: return launch_decode_dv<32>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, flags, st, slots);
+    case 64: return launch_decode_dv<64>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, flags, st, slots);
+    case 128: return launch_decode_dv<128>(dv, q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, flags, st, slots);
   }
   return GDN_ERR_UNSUPPORTED;
 }
+
+GDN_DEFINE_STATUS_GATHER(gather_status_decode)
 
 }  // namespace gdn

@@ -32,9 +32,14 @@ __global__ void bounded_wait_selftest_kernel(int32_t* status, long long max_cycl
   if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
   __syncthreads();
   const bool completed = tc::mbar_wait(&bar, 0, max_cycles);
-  if (threadIdx.x == 0) *status = completed ? GDN_OK : GDN_ERR_TIMEOUT;
+  if (threadIdx.x == 0) {
+    *status = completed ? GDN_OK : GDN_ERR_TIMEOUT;
+    if (!completed) record_device_status(GDN_ERR_TIMEOUT);
+  }
 }
 }  // namespace
+
+GDN_DEFINE_STATUS_GATHER(gather_status_api)
 }  // namespace gdn
 
 using namespace gdn;
@@ -47,6 +52,17 @@ gdn_status_t gdn_selftest_bounded_wait(int32_t* device_status, int64_t max_cycle
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       device_status, (long long)max_cycles);
   return check_launch();
+}
+
+gdn_status_t gdn_device_status(int32_t* status, int32_t clear, void* stream) {
+  if (!status || (clear != 0 && clear != 1)) return GDN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(status) & 3u) != 0) return GDN_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gdn_status_t rc;
+  if ((rc = gather_status_api(status, clear, 1, st)) != GDN_OK) return rc;
+  if ((rc = gather_status_conv(status, clear, 0, st)) != GDN_OK) return rc;
+  if ((rc = gather_status_decode(status, clear, 0, st)) != GDN_OK) return rc;
+  return gather_status_prefill_tc(status, clear, 0, st);
 }
 
 const char* gdn_status_string(gdn_status_t s) {
@@ -185,9 +201,9 @@ static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_
                                        const void* v, int64_t v_stride, const float* a,
                                        const float* b, const float* S, const void* o,
                                        int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                       int32_t qk_l2norm) {
+                                       int32_t flags) {
   if (!q || !k || !v || !a || !b || !S || !o) return GDN_ERR_INVALID_ARG;
-  if (Hk <= 0 || Hv <= 0 || (qk_l2norm != 0 && qk_l2norm != 1)) return GDN_ERR_INVALID_ARG;
+  if (Hk <= 0 || Hv <= 0 || (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_GATE_LOGITS)) != 0) return GDN_ERR_INVALID_ARG;
   if (Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
   if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
   if (qk_stride < (int64_t)Hk * dk || v_stride < (int64_t)Hv * dv) return GDN_ERR_INVALID_ARG;
@@ -200,23 +216,23 @@ static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_
 static gdn_status_t decode_impl(const void* q, const void* k, int64_t qk_stride, const void* v,
                                 int64_t v_stride, const float* a, const float* b, float* S,
                                 void* o, int32_t N, int32_t Hk, int32_t Hv, int32_t dk,
-                                int32_t dv, int32_t qk_l2norm, void* stream, StateSlots slots) {
+                                int32_t dv, int32_t flags, void* stream, StateSlots slots) {
   if (N < 0) return GDN_ERR_INVALID_ARG;
   if (N == 0) return GDN_OK;
   gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
-                                       qk_l2norm);
+                                       flags);
   if (rc != GDN_OK) return rc;
   if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
   return launch_delta_decode(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv,
-                             qk_l2norm, static_cast<cudaStream_t>(stream), slots);
+                             flags, static_cast<cudaStream_t>(stream), slots);
 }
 
 gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t qk_stride,
                                    const void* v, int64_t v_stride, const float* a,
                                    const float* b, float* S, void* o, int32_t N,
                                    int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                   int32_t qk_l2norm, void* stream) {
-  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, qk_l2norm,
+                                   int32_t flags, void* stream) {
+  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, flags,
                      stream, StateSlots{});
 }
 
@@ -224,12 +240,12 @@ gdn_status_t gdn_delta_rule_decode_slots(const void* q, const void* k, int64_t q
                                          const void* v, int64_t v_stride, const float* a,
                                          const float* b, float* S, void* o, int32_t N,
                                          int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                         int32_t qk_l2norm, const int32_t* state_indices,
+                                         int32_t flags, const int32_t* state_indices,
                                          int32_t num_slots, void* stream) {
   StateSlots slots;
   gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
   if (rc != GDN_OK) return rc;
-  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, qk_l2norm,
+  return decode_impl(q, k, qk_stride, v, v_stride, a, b, S, o, N, Hk, Hv, dk, dv, flags,
                      stream, slots);
 }
 
@@ -238,13 +254,13 @@ gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* 
                                    void* conv_state_out, const float* a, const float* b,
                                    float* S, void* o, int32_t N, int32_t Hk, int32_t Hv,
                                    int32_t dk, int32_t dv, int32_t K, int32_t silu,
-                                   int32_t qk_l2norm, void* stream) {
+                                   int32_t flags, void* stream) {
   if (N < 0) return GDN_ERR_INVALID_ARG;
   if (N == 0) return GDN_OK;
   if (!x || !w || !conv_state_in || !conv_state_out || !a || !b || !S || !o)
     return GDN_ERR_INVALID_ARG;
   if (Hk <= 0 || Hv <= 0 || Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
-  if ((silu != 0 && silu != 1) || (qk_l2norm != 0 && qk_l2norm != 1)) return GDN_ERR_INVALID_ARG;
+  if ((silu != 0 && silu != 1) || (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_GATE_LOGITS)) != 0) return GDN_ERR_INVALID_ARG;
   if (K != kConvTaps) return GDN_ERR_UNSUPPORTED;
   if (dk != 128 || dv != 128) return GDN_ERR_UNSUPPORTED;
   const int64_t C = 2 * (int64_t)Hk * dk + (int64_t)Hv * dv;
@@ -259,7 +275,7 @@ gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* 
   const uintptr_t sb = (uintptr_t)N * (uintptr_t)C * 3u * 2u;
   if (si < so + sb && so < si + sb) return GDN_ERR_INVALID_ARG;   // the states overlap
   return launch_decode_fused(x, x_stride, w, bias, conv_state_in, conv_state_out, a, b, S, o, N,
-                             Hk, Hv, silu, qk_l2norm, static_cast<cudaStream_t>(stream));
+                             Hk, Hv, silu, flags, static_cast<cudaStream_t>(stream));
 }
 
 size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32_t Hv, int32_t dk,
@@ -274,7 +290,7 @@ gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride,
                                 int64_t v_stride, const float* a, const float* b,
                                 const int32_t* cu_seqlens, int32_t N, int32_t T, const float* S,
                                 const void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                int32_t chunk, int32_t qk_l2norm, bool* nothing_to_do) {
+                                int32_t chunk, int32_t flags, bool* nothing_to_do) {
   *nothing_to_do = false;
   if (T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
   if (chunk != 64) return GDN_ERR_UNSUPPORTED;
@@ -284,7 +300,7 @@ gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride,
   }
   if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
   gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
-                                       qk_l2norm);
+                                       flags);
   if (rc != GDN_OK) return rc;
   if (dk != dv) return GDN_ERR_UNSUPPORTED;
   return GDN_OK;
@@ -298,17 +314,17 @@ static gdn_status_t prefill_impl(const void* q, const void* k, int64_t qk_stride
                                  const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
                                  const uint8_t* has_initial_state, void* o, int32_t Hk,
                                  int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
-                                 int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+                                 int32_t flags, void* workspace, size_t workspace_bytes,
                                  void* stream, StateSlots slots) {
   bool nothing = false;
   gdn_status_t rc = check_prefill_args(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                                       o, Hk, Hv, dk, dv, chunk, qk_l2norm, &nothing);
+                                       o, Hk, Hv, dk, dv, chunk, flags, &nothing);
   if (rc != GDN_OK || nothing) return rc;
   const size_t need = prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
   if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
   return launch_delta_prefill(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                              has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                              has_initial_state, o, Hk, Hv, dk, dv, chunk, flags, workspace,
                               static_cast<cudaStream_t>(stream), slots);
 }
 
@@ -318,11 +334,11 @@ gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_
                                             const int32_t* cu_seqlens, int32_t N, int32_t T,
                                             float* S, const uint8_t* has_initial_state,
                                             void* o, int32_t Hk, int32_t Hv, int32_t dk,
-                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
+                                            int32_t dv, int32_t chunk, int32_t flags,
                                             void* workspace, size_t workspace_bytes,
                                             void* stream) {
   return prefill_impl(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                      has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                      has_initial_state, o, Hk, Hv, dk, dv, chunk, flags, workspace,
                       workspace_bytes, stream, StateSlots{});
 }
 
@@ -330,13 +346,13 @@ gdn_status_t gdn_delta_rule_prefill_chunked_slots(
     const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
     const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-    int32_t chunk, int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+    int32_t chunk, int32_t flags, void* workspace, size_t workspace_bytes,
     const int32_t* state_indices, int32_t num_slots, void* stream) {
   StateSlots slots;
   gdn_status_t rc = make_slots(state_indices, num_slots, &slots);
   if (rc != GDN_OK) return rc;
   return prefill_impl(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                      has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm, workspace,
+                      has_initial_state, o, Hk, Hv, dk, dv, chunk, flags, workspace,
                       workspace_bytes, stream, slots);
 }
 

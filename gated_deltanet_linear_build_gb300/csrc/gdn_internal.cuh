@@ -8,8 +8,50 @@
 #include <utility>
 
 #include "gdn.h"
+#include "tc_ptx.cuh"
 
 namespace gdn {
+
+// ---------------------------------------------------------------------------
+// Sticky device-side status. Every translation unit that includes this header
+// owns one word (anonymous namespace: no cross-unit device symbols are needed,
+// so no device link step). A kernel whose bounded wait gives up records
+// GDN_ERR_TIMEOUT there (the first failure since the last clear stays);
+// gdn_device_status reads the words of all units through their gather kernels.
+// ---------------------------------------------------------------------------
+namespace {
+__device__ int32_t g_dev_status = 0;
+__global__ void gather_status_kernel(int32_t* out, int clear, int first) {
+  const int32_t v = *reinterpret_cast<volatile int32_t*>(&g_dev_status);
+  if (first || *out == GDN_OK) *out = v;
+  if (clear) g_dev_status = GDN_OK;
+}
+}  // namespace
+__device__ __forceinline__ void record_device_status(int32_t status) {
+  atomicCAS(&g_dev_status, (int32_t)GDN_OK, status);
+}
+
+// Bounded mbarrier wait for the phase of parity `parity` that also gives up as
+// soon as *abort is non-zero (another role of the CTA gave up). On its own
+// time-out (about `max_cycles` SM cycles) it sets *abort and records
+// GDN_ERR_TIMEOUT in the sticky status. `sleep_ns` > 0 backs off between
+// polls, so that a waiting warp takes few issue slots. Returns true when the
+// phase completed.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* mbar, uint32_t parity,
+                                                    volatile int* abort, unsigned sleep_ns = 0,
+                                                    long long max_cycles = 4000000000LL) {
+  const long long t0 = clock64();
+  while (!tc::mbar_try_wait(mbar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > max_cycles) {
+      *abort = 1;
+      record_device_status(GDN_ERR_TIMEOUT);
+      return false;
+    }
+    if (sleep_ns) __nanosleep(sleep_ns);
+  }
+  return true;
+}
 
 // ---------------------------------------------------------------------------
 // BF16 <-> float32 on packed 32-bit words (two BF16 values, element 0 in the
@@ -106,6 +148,39 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 }
 
 // ---------------------------------------------------------------------------
+// Option bits of the delta-rule entry points' `flags` (GDN_FLAG_* in gdn.h).
+// ---------------------------------------------------------------------------
+constexpr int kFlagL2 = GDN_FLAG_QK_L2NORM;
+constexpr int kFlagGateLogits = GDN_FLAG_GATE_LOGITS;
+
+// Gate activation from raw logits: a = exp(-softplus(z)) (decay), b =
+// sigmoid(z) (write strength), with softplus(z) = max(z, 0) + log(1 + e^-|z|)
+// so that no intermediate overflows. Decays below 1e-30 act as 1e-30 in both
+// gate forms (the kernels work with log a).
+__device__ __forceinline__ float softplus_f(float z) {
+  return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
+}
+// log2 of the decay, clamped at log2(1e-30).
+__device__ __forceinline__ float gate_log2_decay(float x, bool logits) {
+  constexpr float kLog2Min = -99.65784284662087f;   // log2(1e-30)
+  return logits ? fmaxf(-softplus_f(x) * 1.4426950408889634f, kLog2Min)
+                : log2f(fmaxf(x, 1e-30f));
+}
+// Natural log of the decay, clamped at ln(1e-30).
+__device__ __forceinline__ float gate_ln_decay(float x, bool logits) {
+  constexpr float kLnMin = -69.07755278982137f;     // ln(1e-30)
+  return logits ? fmaxf(-softplus_f(x), kLnMin) : logf(fmaxf(x, 1e-30f));
+}
+// The decay itself (decode forms).
+__device__ __forceinline__ float gate_decay(float x, bool logits) {
+  return logits ? expf(-softplus_f(x)) : x;
+}
+// The write strength.
+__device__ __forceinline__ float gate_write(float x, bool logits) {
+  return logits ? 1.0f / (1.0f + expf(-x)) : x;
+}
+
+// ---------------------------------------------------------------------------
 // Host-side helpers
 // ---------------------------------------------------------------------------
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -188,6 +263,19 @@ __device__ __forceinline__ int state_slot(const StateSlots& s, int n) {
   return (v >= 0 && v < s.count) ? v : -1;
 }
 
+// Status gathers of the kernel translation units (each launches its unit's
+// gather_status_kernel): the first one called writes its word, the others only
+// replace a GDN_OK.
+gdn_status_t gather_status_api(int32_t* out, int clear, int first, cudaStream_t st);
+gdn_status_t gather_status_conv(int32_t* out, int clear, int first, cudaStream_t st);
+gdn_status_t gather_status_decode(int32_t* out, int clear, int first, cudaStream_t st);
+gdn_status_t gather_status_prefill_tc(int32_t* out, int clear, int first, cudaStream_t st);
+#define GDN_DEFINE_STATUS_GATHER(name)                                                   \
+  gdn_status_t name(int32_t* out, int clear, int first, cudaStream_t st) {               \
+    gather_status_kernel<<<1, 1, 0, st>>>(out, clear, first);                            \
+    return check_launch();                                                               \
+  }
+
 // Launchers implemented in the kernel translation units. They assume their
 // arguments were validated by the C ABI layer.
 gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
@@ -207,14 +295,14 @@ gdn_status_t launch_conv_update(const void* x, int64_t x_stride, const void* w,
 gdn_status_t launch_delta_decode(const void* q, const void* k, int64_t qk_stride,
                                  const void* v, int64_t v_stride, const float* a,
                                  const float* b, float* S, void* o, int32_t N, int32_t Hk,
-                                 int32_t Hv, int32_t dk, int32_t dv, int32_t qk_l2norm,
+                                 int32_t Hv, int32_t dk, int32_t dv, int32_t flags,
                                  cudaStream_t st, StateSlots slots = {});
 
 // Conv update and delta-rule decode in one launch (dk = dv = 128).
 gdn_status_t launch_decode_fused(const void* x, int64_t x_stride, const void* w,
                                  const void* bias, const void* st_in, void* st_out,
                                  const float* a, const float* b, float* S, void* o, int32_t N,
-                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t qk_l2norm,
+                                 int32_t Hk, int32_t Hv, int32_t silu, int32_t flags,
                                  cudaStream_t st);
 
 size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int32_t dv,
@@ -227,14 +315,14 @@ gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride,
                                 int64_t v_stride, const float* a, const float* b,
                                 const int32_t* cu_seqlens, int32_t N, int32_t T, const float* S,
                                 const void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                int32_t chunk, int32_t qk_l2norm, bool* nothing_to_do);
+                                int32_t chunk, int32_t flags, bool* nothing_to_do);
 
 gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_stride,
                                   const void* v, int64_t v_stride, const float* a,
                                   const float* b, const int32_t* cu, int32_t N, int32_t T,
                                   float* S, const uint8_t* has_init, void* o, int32_t Hk,
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
-                                  int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                                  int32_t flags, void* workspace, cudaStream_t st,
                                   StateSlots slots = {});
 
 // Tensor-core (tcgen05) chunked prefill for dk = dv = 128.
@@ -243,7 +331,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
                                int64_t v_stride, const float* a, const float* b,
                                const int32_t* cu, int32_t N, int32_t T, float* S,
                                const uint8_t* has_init, void* o, int32_t Hk, int32_t Hv,
-                               int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                               int32_t flags, void* workspace, cudaStream_t st,
                                StateSlots slots = {});
 
 }  // namespace gdn

@@ -95,7 +95,7 @@ intra_chunk_kernel(const __nv_bfloat16* __restrict__ k, int64_t qk_stride,
                    const __nv_bfloat16* __restrict__ v, int64_t v_stride,
                    const float* __restrict__ a, const float* __restrict__ b,
                    const int32_t* __restrict__ count, const gdn_conv_chunk_t* __restrict__ desc,
-                   int T, int Hk, int Hv, int qk_l2norm, float* __restrict__ g_ws,
+                   int T, int Hk, int Hv, int flags, float* __restrict__ g_ws,
                    float* __restrict__ w_ws, float* __restrict__ u_ws) {
   constexpr int PK = DK + 1, PV = DV + 1, PT = kChunk + 1;
   extern __shared__ float smem[];
@@ -114,12 +114,13 @@ intra_chunk_kernel(const __nv_bfloat16* __restrict__ k, int64_t qk_stride,
   const int h = blockIdx.y, g = h / (Hv / Hk);
   const int tid = threadIdx.x;
 
-  load_rows_bf16<DK, PK>(Ks, k + tok0 * qk_stride + (int64_t)g * DK, qk_stride, n, qk_l2norm);
+  load_rows_bf16<DK, PK>(Ks, k + tok0 * qk_stride + (int64_t)g * DK, qk_stride, n, flags & kFlagL2);
   load_rows_bf16<DV, PV>(Vs, v + tok0 * v_stride + (int64_t)h * DV, v_stride, n, 0);
   if (tid < kChunk) {
     const bool in = tid < n;
-    gs[tid] = in ? logf(fmaxf(a[(int64_t)(tok0 + tid) * Hv + h], 1e-30f)) : 0.f;
-    bs[tid] = in ? b[(int64_t)(tok0 + tid) * Hv + h] : 0.f;
+    const bool gl = (flags & kFlagGateLogits) != 0;
+    gs[tid] = in ? gate_ln_decay(a[(int64_t)(tok0 + tid) * Hv + h], gl) : 0.f;
+    bs[tid] = in ? gate_write(b[(int64_t)(tok0 + tid) * Hv + h], gl) : 0.f;
   }
   __syncthreads();
   if (tid == 0) {
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(kThreads)
 state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                   int64_t qk_stride, const int32_t* __restrict__ cu, int T,
                   float* __restrict__ S, const uint8_t* __restrict__ has_init,
-                  __nv_bfloat16* __restrict__ o, int Hk, int Hv, int qk_l2norm,
+                  __nv_bfloat16* __restrict__ o, int Hk, int Hv, int flags,
                   const float* __restrict__ g_ws, const float* __restrict__ w_ws,
                   const float* __restrict__ u_ws, const int32_t* __restrict__ bstatus,
                   const StateSlots slots) {
@@ -210,8 +211,8 @@ state_pass_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __re
   for (int c0 = start; c0 < end; c0 += kChunk) {
     const int n = min(kChunk, end - c0);
     __syncthreads();
-    load_rows_bf16<DK, PK>(Qs, q + c0 * qk_stride + (int64_t)g * DK, qk_stride, n, qk_l2norm);
-    load_rows_bf16<DK, PK>(Ks, k + c0 * qk_stride + (int64_t)g * DK, qk_stride, n, qk_l2norm);
+    load_rows_bf16<DK, PK>(Qs, q + c0 * qk_stride + (int64_t)g * DK, qk_stride, n, flags & kFlagL2);
+    load_rows_bf16<DK, PK>(Ks, k + c0 * qk_stride + (int64_t)g * DK, qk_stride, n, flags & kFlagL2);
     for (int idx = tid; idx < kChunk * DK; idx += kThreads) {
       const int r = idx / DK, j = idx % DK;
       Ws[r * PK + j] = r < n ? w_ws[((int64_t)(c0 + r) * Hv + h) * DK + j] : 0.f;
@@ -275,7 +276,7 @@ template <int D>
 gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, const void* v,
                               int64_t v_stride, const float* a, const float* b,
                               const int32_t* cu, int N, int T, float* S,
-                              const uint8_t* has_init, void* o, int Hk, int Hv, int l2,
+                              const uint8_t* has_init, void* o, int Hk, int Hv, int flags,
                               void* workspace, cudaStream_t st, StateSlots slots) {
   constexpr int DK = D, DV = D, SL = D < kSlice ? D : kSlice;
   const WsLayout L = ws_layout(T, N, Hv, DK, DV);
@@ -314,10 +315,10 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   }();
   (void)smem_attrs;
   k1<<<dim3(L.capacity, Hv), kThreads, smem1, st>>>(kp, qk_stride, vp, v_stride, a, b, count,
-                                                     desc, T, Hk, Hv, l2, g_ws, w_ws, u_ws);
+                                                     desc, T, Hk, Hv, flags, g_ws, w_ws, u_ws);
   if ((rc = check_launch()) != GDN_OK) return rc;
   k2<<<dim3(N, Hv, DV / SL), kThreads, smem2, st>>>(qp, kp, qk_stride, cu, T, S, has_init,
-                                                    static_cast<__nv_bfloat16*>(o), Hk, Hv, l2,
+                                                    static_cast<__nv_bfloat16*>(o), Hk, Hv, flags,
                                                     g_ws, w_ws, u_ws, bstatus, slots);
   return check_launch();
 }
@@ -336,15 +337,15 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
                                   const float* b, const int32_t* cu, int32_t N, int32_t T,
                                   float* S, const uint8_t* has_init, void* o, int32_t Hk,
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
-                                  int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                                  int32_t flags, void* workspace, cudaStream_t st,
                                   StateSlots slots) {
   (void)chunk;
   if (dk != dv) return GDN_ERR_UNSUPPORTED;
   switch (dk) {
-    case 16: return launch_prefill_t<16>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
-    case 32: return launch_prefill_t<32>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
-    case 64: return launch_prefill_t<64>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
-    case 128: return launch_prefill_tc(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, qk_l2norm, workspace, st, slots);
+    case 16: return launch_prefill_t<16>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, flags, workspace, st, slots);
+    case 32: return launch_prefill_t<32>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, flags, workspace, st, slots);
+    case 64: return launch_prefill_t<64>(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, flags, workspace, st, slots);
+    case 128: return launch_prefill_tc(q, k, qk_stride, v, v_stride, a, b, cu, N, T, S, has_init, o, Hk, Hv, flags, workspace, st, slots);
   }
   return GDN_ERR_UNSUPPORTED;
 }

@@ -121,12 +121,12 @@ extern "C" gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
     const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
     const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-    int32_t chunk, int32_t qk_l2norm, void* stream) {
+    int32_t chunk, int32_t flags, void* stream) {
   // Every argument check and the size limit come first, so a rejected call
   // touches no CUDA state at all (no context set-up, no symbol lookup).
   bool nothing = false;
   gdn_status_t rc = check_prefill_args(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                                       o, Hk, Hv, dk, dv, chunk, qk_l2norm, &nothing);
+                                       o, Hk, Hv, dk, dv, chunk, flags, &nothing);
   if (rc != GDN_OK || nothing) return rc;
   const size_t need = gdn_delta_rule_prefill_workspace_size(T, N, Hv, dk, dv, chunk);
   if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
@@ -134,7 +134,7 @@ extern "C" gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
   rc = scratch_address(&scratch);
   if (rc != GDN_OK) return rc;
   return gdn_delta_rule_prefill_chunked(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
-                                        has_initial_state, o, Hk, Hv, dk, dv, chunk, qk_l2norm,
+                                        has_initial_state, o, Hk, Hv, dk, dv, chunk, flags,
                                         scratch, kNoAllocScratchBytes, stream);
 }
 

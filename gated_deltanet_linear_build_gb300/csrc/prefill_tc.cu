@@ -166,7 +166,7 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
                 int64_t qk_stride, const __nv_bfloat16* __restrict__ v, int64_t v_stride,
                 const float* __restrict__ a, const float* __restrict__ b,
                 const int32_t* __restrict__ hdr, const gdn_conv_chunk_t* __restrict__ desc,
-                int T, int Hk, int Hv, int l2, unsigned char* __restrict__ records,
+                int T, int Hk, int Hv, int flags, unsigned char* __restrict__ records,
                 int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   float* Af = reinterpret_cast<float*>(sm + kS1_AF);
@@ -225,8 +225,9 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
   if (tid < 64) {
     const bool in = tid < n;
     // log2 of the decay, so that decay ratios are single exp2 evaluations.
-    float x = in ? log2f(fmaxf(a[(int64_t)(tok0 + tid) * Hv + h], 1e-30f)) : 0.f;
-    bs[tid] = in ? b[(int64_t)(tok0 + tid) * Hv + h] : 0.f;
+    const bool gl = (flags & kFlagGateLogits) != 0;
+    float x = in ? gate_log2_decay(a[(int64_t)(tok0 + tid) * Hv + h], gl) : 0.f;
+    bs[tid] = in ? gate_write(b[(int64_t)(tok0 + tid) * Hv + h], gl) : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -248,7 +249,7 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
     }
-    const float r = l2 ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    const float r = (flags & kFlagL2) ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     if (tid < 64) rk[tid] = r; else rq[tid - 64] = r;
   }
   fence_smem_to_async();
@@ -436,6 +437,7 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
     fence_smem_to_async();
   } else if (tid == 0) {
     atomicExch(status + 2, (int)GDN_ERR_TIMEOUT);
+    record_device_status(GDN_ERR_TIMEOUT);
   }
   fence_before_sync();
   __syncthreads();
@@ -627,7 +629,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       }
     }
     // Bounded, not abortable: the MMAs in flight must finish before exit.
-    if (lane == 0 && issued) mbar_wait(bO1, last_par);
+    if (lane == 0 && issued && !mbar_wait(bO1, last_par)) record_device_status(GDN_ERR_TIMEOUT);
     __syncwarp();
   } else if (warp == 11) {
     // ---------------- K rows (warp 11) ----------------
@@ -676,9 +678,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     }
     if (lane == 0) {
       // Bounded, not abortable: copies in flight must land before exit.
-      if (pend_w >= 0) mbar_wait(bW, pend_w & 1);
-      if (pend_u >= 0) mbar_wait(bU, pend_u & 1);
-      if (pend_p >= 0) mbar_wait(bP, pend_p & 1);
+      bool drained = true;
+      if (pend_w >= 0) drained = mbar_wait(bW, pend_w & 1) && drained;
+      if (pend_u >= 0) drained = mbar_wait(bU, pend_u & 1) && drained;
+      if (pend_p >= 0) drained = mbar_wait(bP, pend_p & 1) && drained;
+      if (!drained) record_device_status(GDN_ERR_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == 8) {
@@ -724,7 +728,7 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
       }
       // Bounded, not abortable: the MMAs in flight must finish before exit.
-      if (last != nullptr) mbar_wait(last, last_par);
+      if (last != nullptr && !mbar_wait(last, last_par)) record_device_status(GDN_ERR_TIMEOUT);
     }
     __syncwarp();
   } else {
@@ -920,8 +924,10 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
       }
     }
-    if (tid == 0 && (failed() || !records_ok))
+    if (tid == 0 && (failed() || !records_ok)) {
       atomicExch(hdr + 2, (int)(failed() ? GDN_ERR_TIMEOUT : GDN_ERR_INVALID_ARG));
+      if (failed()) record_device_status(GDN_ERR_TIMEOUT);
+    }
     __syncwarp();
   }
   cp_async_wait_all();
@@ -940,7 +946,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
                                int64_t v_stride, const float* a, const float* b,
                                const int32_t* cu, int32_t N, int32_t T, float* S,
                                const uint8_t* has_init, void* o, int32_t Hk, int32_t Hv,
-                               int32_t qk_l2norm, void* workspace, cudaStream_t st,
+                               int32_t flags, void* workspace, cudaStream_t st,
                                StateSlots slots) {
   const TcLayout L = tc_layout(T, N, Hv);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -960,7 +966,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
            tc_chunk_kernel, dim3(L.capacity, Hv), dim3(kThreads), kS1_BYTES, st,
            static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(q), qk_stride,
            static_cast<const __nv_bfloat16*>(v), v_stride, a, b, (const int32_t*)hdr, desc, T, Hk,
-           Hv, qk_l2norm, records, hdr))) != GDN_OK)
+           Hv, flags, records, hdr))) != GDN_OK)
     return rc;
   return check_launch(launch_pdl(
       tc_state_kernel, dim3(N, Hv), dim3(kThreads2), kS2_BYTES, st,
@@ -968,5 +974,7 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
       T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, (const unsigned char*)records,
       hdr, slots));
 }
+
+GDN_DEFINE_STATUS_GATHER(gather_status_prefill_tc)
 
 }  // namespace gdn

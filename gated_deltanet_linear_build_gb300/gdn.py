@@ -23,6 +23,10 @@ GDN_ERR_WORKSPACE = -4
 GDN_ERR_CUDA = -5
 GDN_ERR_TIMEOUT = -6
 
+# Option bits of the delta-rule calls' flags argument (GDN_FLAG_* in gdn.h).
+GDN_FLAG_QK_L2NORM = 1
+GDN_FLAG_GATE_LOGITS = 2
+
 # Every symbol that include/gdn.h declares.
 EXPORTED_SYMBOLS = (
     "gdn_build_conv_chunks",
@@ -39,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "gdn_delta_rule_decode_slots",
     "gdn_delta_rule_prefill_chunked_slots",
     "gdn_selftest_bounded_wait",
+    "gdn_device_status",
     "gdn_status_string",
     "gdn_last_cuda_error_string",
 )
@@ -89,6 +94,7 @@ _SIGNATURES = {
                                                             _I32, _I32, _I32, _I32, _P,
                                                             ctypes.c_size_t, _P, _I32, _P]),
     "gdn_selftest_bounded_wait": (ctypes.c_int, [_P, _I64, _P]),
+    "gdn_device_status": (ctypes.c_int, [_P, _I32, _P]),
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_last_cuda_error_string": (ctypes.c_char_p, []),
 }
@@ -124,6 +130,10 @@ def _stream(stream=None):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _flags(qk_l2norm: bool, gate_logits: bool) -> int:
+    return (GDN_FLAG_QK_L2NORM if qk_l2norm else 0) | (GDN_FLAG_GATE_LOGITS if gate_logits else 0)
 
 
 def _check(rc: int, fn: str):
@@ -174,21 +184,22 @@ def causal_conv1d_update(x, w, bias, conv_state, y, *, silu: bool = True, stream
     _check(rc, "gdn_causal_conv1d_update")
 
 
-def delta_rule_decode(q, k, v, a, b, S, o, *, qk_l2norm: bool = False, stream=None):
+def delta_rule_decode(q, k, v, a, b, S, o, *, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     """Decode update. q, k [N, Hk, dk] (token stride q.stride(0), heads
-    contiguous), v [N, Hv, dv], a, b [N, Hv] float32, S [N, Hv, dv, dk] float32
-    (in place), o [N, Hv, dv]."""
+    contiguous), v [N, Hv, dv], a, b [N, Hv] float32 (activated gates, or their
+    logits with gate_logits=True: the kernel then computes a = exp(-softplus(a)),
+    b = sigmoid(b)), S [N, Hv, dv, dk] float32 (in place), o [N, Hv, dv]."""
     N, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     assert k.stride(0) == q.stride(0), "q and k share one token stride"
     rc = _lib().gdn_delta_rule_decode(_ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0),
                                       _ptr(a), _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk, dv,
-                                      int(qk_l2norm), _stream(stream))
+                                      _flags(qk_l2norm, gate_logits), _stream(stream))
     _check(rc, "gdn_delta_rule_decode")
 
 
 def decode_step_fused(x, w, bias, conv_state_in, conv_state_out, a, b, S, o, *, Hk: int,
-                      silu: bool = True, qk_l2norm: bool = False, stream=None):
+                      silu: bool = True, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     """Conv update and delta-rule decode in one launch. x [N, C] conv inputs
     (C = 2 Hk d + Hv d), conv_state_in / conv_state_out [N, C, 3] (distinct
     buffers), a, b [N, Hv], S [N, Hv, d, d] (in place), o [N, Hv, d]."""
@@ -197,7 +208,7 @@ def decode_step_fused(x, w, bias, conv_state_in, conv_state_out, a, b, S, o, *, 
     rc = _lib().gdn_decode_step_fused(_ptr(x), x.stride(0), _ptr(w), _ptr(bias),
                                       _ptr(conv_state_in), _ptr(conv_state_out), _ptr(a),
                                       _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk, dv, w.shape[1],
-                                      int(silu), int(qk_l2norm), _stream(stream))
+                                      int(silu), _flags(qk_l2norm, gate_logits), _stream(stream))
     _check(rc, "gdn_decode_step_fused")
 
 
@@ -207,7 +218,7 @@ def delta_rule_prefill_workspace_size(T: int, N: int, Hv: int, dk: int, dv: int,
 
 
 def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, o, workspace,
-                               *, chunk: int = 64, qk_l2norm: bool = False, stream=None):
+                               *, chunk: int = 64, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     """Chunked prefill over packed sequences. q, k [T, Hk, dk]; v [T, Hv, dv];
     a, b [T, Hv]; cu_seqlens [N+1]; S [N, Hv, dv, dk] (initial in, final out);
     has_initial_state uint8 [N] or None; o [T, Hv, dv]; workspace uint8 tensor
@@ -220,12 +231,12 @@ def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, 
     rc = _lib().gdn_delta_rule_prefill_chunked(
         _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
-        chunk, int(qk_l2norm), _ptr(workspace), nbytes, _stream(stream))
+        chunk, _flags(qk_l2norm, gate_logits), _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked")
 
 
 def delta_rule_prefill_chunked_noalloc(q, k, v, a, b, cu_seqlens, S, has_initial_state, o, *,
-                                       chunk: int = 64, qk_l2norm: bool = False, stream=None):
+                                       chunk: int = 64, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     """The chunked prefill without a workspace argument, for callers that may
     not allocate device memory: scratch is the library's fixed 64 MiB device
     array. Same arguments and results as delta_rule_prefill_chunked. Calls
@@ -237,7 +248,7 @@ def delta_rule_prefill_chunked_noalloc(q, k, v, a, b, cu_seqlens, S, has_initial
     rc = _lib().gdn_delta_rule_prefill_chunked_noalloc(
         _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
-        chunk, int(qk_l2norm), _stream(stream))
+        chunk, _flags(qk_l2norm, gate_logits), _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked_noalloc")
 
 
@@ -282,21 +293,21 @@ def causal_conv1d_update_slots(x, w, bias, conv_state, y, state_indices, *, num_
 
 
 def delta_rule_decode_slots(q, k, v, a, b, S, o, state_indices, *, num_slots=None,
-                            qk_l2norm: bool = False, stream=None):
+                            qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     N, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     assert k.stride(0) == q.stride(0), "q and k share one token stride"
     ns = S.shape[0] if num_slots is None else num_slots
     rc = _lib().gdn_delta_rule_decode_slots(_ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0),
                                             _ptr(a), _ptr(b), _ptr(S), _ptr(o), N, Hk, Hv, dk,
-                                            dv, int(qk_l2norm), _ptr(state_indices), ns,
+                                            dv, _flags(qk_l2norm, gate_logits), _ptr(state_indices), ns,
                                             _stream(stream))
     _check(rc, "gdn_delta_rule_decode_slots")
 
 
 def delta_rule_prefill_chunked_slots(q, k, v, a, b, cu_seqlens, S, has_initial_state, o,
                                      workspace, state_indices, *, num_slots=None,
-                                     chunk: int = 64, qk_l2norm: bool = False, stream=None):
+                                     chunk: int = 64, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
     T, Hk, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -306,7 +317,7 @@ def delta_rule_prefill_chunked_slots(q, k, v, a, b, cu_seqlens, S, has_initial_s
     rc = _lib().gdn_delta_rule_prefill_chunked_slots(
         _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
-        chunk, int(qk_l2norm), _ptr(workspace), nbytes, _ptr(state_indices), ns, _stream(stream))
+        chunk, _flags(qk_l2norm, gate_logits), _ptr(workspace), nbytes, _ptr(state_indices), ns, _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked_slots")
 
 
@@ -315,6 +326,14 @@ def selftest_bounded_wait(device_status, *, max_cycles: int = 2_000_000, stream=
     library's bounded wait; device_status int32 [1] becomes GDN_ERR_TIMEOUT."""
     rc = _lib().gdn_selftest_bounded_wait(_ptr(device_status), int(max_cycles), _stream(stream))
     _check(rc, "gdn_selftest_bounded_wait")
+
+
+def device_status(status, *, clear: bool = False, stream=None):
+    """Enqueue the read of the library's sticky device status into ``status``
+    (device int32 [1]): GDN_OK, or the first failure a kernel recorded
+    (GDN_ERR_TIMEOUT) since the last clear; ``clear`` resets it."""
+    rc = _lib().gdn_device_status(_ptr(status), int(clear), _stream(stream))
+    _check(rc, "gdn_device_status")
 
 
 def prefill_workspace_status(workspace):

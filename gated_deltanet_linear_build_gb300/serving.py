@@ -7,6 +7,7 @@ synthetic one, the same for every layer:
 
     x = bf16(h / sqrt(mean(h^2) + 1e-6))                       (per token)
     a = exp(-softplus(u_h . x_v[h] / sqrt(d))),  b = sigmoid(r_h . x_v[h] / sqrt(d))
+                                             (activated inside the delta-rule kernels)
     y = causal conv1d + SiLU of x (BF16);   q | k | v = y
     o = gated delta rule (q, k L2-normalised; BF16 output)
     h = h + s * [o, o]                       (o repeated to the stream width)
@@ -24,7 +25,6 @@ import math
 
 import numpy as np
 import torch
-import torch.nn.functional as F
 
 from .stack import GdnLayerStack, pack_prefill_steps
 
@@ -70,14 +70,15 @@ class SyntheticServingStack:
         self.conv_w = [_bf16(w, dev) for w in weights["conv_w"]]
 
     def _gates(self, l, x):
+        """Gate logits z_a, z_b (the projections of the model glue); the
+        delta-rule kernels turn them into a = exp(-softplus(z_a)) and
+        b = sigmoid(z_b)."""
         T = x.shape[0]
         xv = x[:, 2 * self.hk * self.d:].float().reshape(T, self.hv, self.d)
         scale = 1.0 / math.sqrt(self.d)
-        za = (xv * self.gate_u[l]).sum(-1) * scale
-        zb = (xv * self.gate_r[l]).sum(-1) * scale
-        a = torch.exp(-F.softplus(za)).contiguous()
-        b = torch.sigmoid(zb).contiguous()
-        return a, b
+        za = ((xv * self.gate_u[l]).sum(-1) * scale).contiguous()
+        zb = ((xv * self.gate_r[l]).sum(-1) * scale).contiguous()
+        return za, zb
 
     def _residual(self, l, h, o):
         o2 = o.reshape(o.shape[0], -1).float()

@@ -11,7 +11,8 @@ tokens per step, 32 concurrent sequences):
 * per prefill step: the exact 8-token conv descriptors are built ONCE and
   reused by every layer; per layer, the conv prefill over the descriptors and
   the chunked delta-rule prefill on q/k/v read in place from the conv output
-  (q/k L2-normalised inside the kernel);
+  (q/k L2-normalised and the gates activated from their logits inside the
+  kernel);
 * per decode step: per layer, the conv update and the delta-rule decode.
 
 Every step of the path runs in the CUDA library; this module only allocates
@@ -79,12 +80,14 @@ class GdnLayerStack:
     Per layer: conv weights [C, 4] BF16, conv_state [n_seqs, C, 3] BF16 and
     S [n_seqs, Hv, d, d] float32. The conv weights are drawn N(0, w_std^2)
     from ``seed`` unless ``conv_weights`` (one [C, 4] tensor per layer) is
-    given.
+    given. With ``gate_logits`` (the default) the layers' gate inputs are the
+    raw logits z_a, z_b and the delta-rule kernels compute a = exp(-softplus(z_a)),
+    b = sigmoid(z_b) themselves; otherwise they are the activated gates.
     """
 
     def __init__(self, layers: int, n_seqs: int, *, hk: int = 16, hv: int = 32, d: int = 128,
                  max_step_tokens: int = 2048, device="cuda", seed: int = 0,
-                 w_std: float = 0.5, conv_weights=None):
+                 w_std: float = 0.5, conv_weights=None, gate_logits: bool = True):
         self.layers, self.n_seqs = layers, n_seqs
         self.hk, self.hv, self.d = hk, hv, d
         self.C = 2 * hk * d + hv * d
@@ -104,6 +107,7 @@ class GdnLayerStack:
                            for _ in range(layers)]
         self.S = [torch.zeros((n_seqs, hv, d, d), dtype=torch.float32, device=self.device)
                   for _ in range(layers)]
+        self.gate_logits = gate_logits
         self.max_step_tokens = max_step_tokens
         self.chunks = torch.empty((max_step_tokens // 8 + n_seqs, 4), dtype=torch.int32,
                                   device=self.device)
@@ -152,7 +156,8 @@ class GdnLayerStack:
         sl = slice(first_slot, first_slot + n)
         q, k, v = self.qkv(y)
         gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, out,
-                                       self.workspace, qk_l2norm=True)
+                                       self.workspace, qk_l2norm=True,
+                                       gate_logits=self.gate_logits)
         self.launches += PREFILL_LAUNCHES
 
     def conv_update_layer(self, l: int, x, y):
@@ -161,7 +166,8 @@ class GdnLayerStack:
 
     def delta_decode_layer(self, l: int, y, a, b, out):
         q, k, v = self.qkv(y)
-        gdn.delta_rule_decode(q, k, v, a, b, self.S[l], out, qk_l2norm=True)
+        gdn.delta_rule_decode(q, k, v, a, b, self.S[l], out, qk_l2norm=True,
+                              gate_logits=self.gate_logits)
         self.launches += 1
 
     def prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, x, a, b, y, out,

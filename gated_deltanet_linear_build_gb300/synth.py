@@ -67,6 +67,14 @@ def unit_rows_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     return bf16_bits(g)
 
 
+def gate_logits(rng: np.random.Generator, shape, shift_a: float = 0.0, scale: float = 1.0):
+    """Raw gate logits (z_a, z_b) in float32: scale * N(0,1), z_a shifted by
+    ``shift_a`` (a negative shift makes the decay exp(-softplus(z_a)) close to 1)."""
+    z1 = rng.standard_normal(shape, dtype=np.float64) * scale + shift_a
+    z2 = rng.standard_normal(shape, dtype=np.float64) * scale
+    return z1.astype(np.float32), z2.astype(np.float32)
+
+
 def gates(rng: np.random.Generator, shape):
     """Gate inputs as the workloads define them, in float32.
 

@@ -53,6 +53,25 @@
 extern "C" {
 #endif
 
+/*
+ * Option bits of the `flags` argument of the delta-rule entry points
+ * (gdn_delta_rule_decode, gdn_decode_step_fused, gdn_delta_rule_prefill_chunked
+ * and their variants). Other bits are GDN_ERR_INVALID_ARG.
+ *
+ * GDN_FLAG_QK_L2NORM: q and k are first replaced by x / sqrt(sum x^2 + 1e-6)
+ *   per head (the post-conv q/k normalisation).
+ * GDN_FLAG_GATE_LOGITS: the gate arrays hold raw logits z_a, z_b instead of
+ *   activated gates, and the kernel computes a = exp(-softplus(z_a)) (decay)
+ *   and b = sigmoid(z_b) (write strength) itself. Source: "RTX 5070 Ti: close
+ *   Qwen3.5-4B TTFT, TPOT, and VRAM gaps vs vLLM", Existing evidence (the gate
+ *   prep between the conv and the recurrence folded into a kernel: the
+ *   post-conv tile).
+ * Without GDN_FLAG_GATE_LOGITS, a and b are the activated gates. Either way a
+ * decay below 1e-30 acts as 1e-30.
+ */
+#define GDN_FLAG_QK_L2NORM 1
+#define GDN_FLAG_GATE_LOGITS 2
+
 /* Status codes. */
 typedef enum gdn_status_t {
   GDN_OK = 0,
@@ -61,7 +80,7 @@ typedef enum gdn_status_t {
   GDN_ERR_ALIGNMENT = -3,   /* a pointer or stride breaks the 16-byte rule */
   GDN_ERR_WORKSPACE = -4,   /* workspace too small, or descriptor capacity exceeded */
   GDN_ERR_CUDA = -5,        /* a CUDA call failed */
-  GDN_ERR_TIMEOUT = -6      /* reserved: a bounded device-side wait gave up */
+  GDN_ERR_TIMEOUT = -6      /* a bounded device-side wait gave up (gdn_device_status) */
 } gdn_status_t;
 
 /*
@@ -171,11 +190,12 @@ GDN_API gdn_status_t gdn_causal_conv1d_update(const void* x, int64_t x_stride, c
  * For sequence n and v-head h with q/k-head g = h / (Hv / Hk):
  *   S' = a S;  u = b (v - S' k);  S_new = S' + u k^T;  o = S_new q,
  * which equals a S (I - b k k^T) + b v k^T and o = S_new q. No 1/sqrt(dk) scale.
- * With qk_l2norm != 0, q and k are first replaced by x / sqrt(sum x^2 + 1e-6).
+ * flags: GDN_FLAG_QK_L2NORM and / or GDN_FLAG_GATE_LOGITS (see above).
  *
  *   q, k       BF16; element (n, g, i) at n * qk_stride + g * dk + i.
  *   v          BF16; element (n, h, i) at n * v_stride + h * dv + i.
- *   a, b       float32 [N, Hv] contiguous.
+ *   a, b       float32 [N, Hv] contiguous: the decay and write gates, or their
+ *              logits with GDN_FLAG_GATE_LOGITS.
  *   S          float32 [N, Hv, dv, dk] contiguous (row i of S is dk-contiguous),
  *              read and written in place.
  *   o          BF16 [N, Hv, dv] contiguous (output).
@@ -185,7 +205,7 @@ GDN_API gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t
                                    const void* v, int64_t v_stride, const float* a,
                                    const float* b, float* S, void* o, int32_t N,
                                    int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                   int32_t qk_l2norm, void* stream);
+                                   int32_t flags, void* stream);
 
 /*
  * One decode step of a GDN layer in a single launch: the conv update of
@@ -209,7 +229,7 @@ GDN_API gdn_status_t gdn_delta_rule_decode(const void* q, const void* k, int64_t
  *                  GDN_ERR_INVALID_ARG.
  *   a, b, S, o     as for gdn_delta_rule_decode (S updated in place).
  *   dk, dv         128 only (else GDN_ERR_UNSUPPORTED; use the two calls).
- *   K              4.   silu, qk_l2norm: 0 or 1.
+ *   K              4.   silu: 0 or 1.   flags: GDN_FLAG_* bits.
  * All pointers 16-byte aligned.
  */
 GDN_API gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, const void* w,
@@ -217,7 +237,7 @@ GDN_API gdn_status_t gdn_decode_step_fused(const void* x, int64_t x_stride, cons
                                    void* conv_state_out, const float* a, const float* b,
                                    float* S, void* o, int32_t N, int32_t Hk, int32_t Hv,
                                    int32_t dk, int32_t dv, int32_t K, int32_t silu,
-                                   int32_t qk_l2norm, void* stream);
+                                   int32_t flags, void* stream);
 
 /*
  * Bytes of device workspace that gdn_delta_rule_prefill_chunked needs for these
@@ -234,7 +254,8 @@ GDN_API size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32
  * last chunk of a sequence may be partial.
  *
  *   q, k, v, qk_stride, v_stride   as for decode, indexed by packed token t.
- *   a, b        float32 [T, Hv].
+ *   a, b        float32 [T, Hv] (gates, or logits with GDN_FLAG_GATE_LOGITS).
+ *   flags       GDN_FLAG_* bits, as for decode.
  *   cu_seqlens  int32 [N + 1].
  *   S           float32 [N, Hv, dv, dk]: the initial state of sequence s where
  *               has_initial_state[s] != 0 (zeros otherwise), replaced by the
@@ -263,7 +284,7 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k
                                             const int32_t* cu_seqlens, int32_t N, int32_t T,
                                             float* S, const uint8_t* has_initial_state,
                                             void* o, int32_t Hk, int32_t Hv, int32_t dk,
-                                            int32_t dv, int32_t chunk, int32_t qk_l2norm,
+                                            int32_t dv, int32_t chunk, int32_t flags,
                                             void* workspace, size_t workspace_bytes,
                                             void* stream);
 
@@ -314,7 +335,7 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
     const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
     const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-    int32_t chunk, int32_t qk_l2norm, void* stream);
+    int32_t chunk, int32_t flags, void* stream);
 
 /*
  * Status words of the last gdn_delta_rule_prefill_chunked_noalloc call in the
@@ -380,14 +401,14 @@ GDN_API gdn_status_t gdn_delta_rule_decode_slots(const void* q, const void* k, i
                                          const void* v, int64_t v_stride, const float* a,
                                          const float* b, float* S, void* o, int32_t N,
                                          int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                         int32_t qk_l2norm, const int32_t* state_indices,
+                                         int32_t flags, const int32_t* state_indices,
                                          int32_t num_slots, void* stream);
 
 GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_slots(
     const void* q, const void* k, int64_t qk_stride, const void* v, int64_t v_stride,
     const float* a, const float* b, const int32_t* cu_seqlens, int32_t N, int32_t T, float* S,
     const uint8_t* has_initial_state, void* o, int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-    int32_t chunk, int32_t qk_l2norm, void* workspace, size_t workspace_bytes,
+    int32_t chunk, int32_t flags, void* workspace, size_t workspace_bytes,
     const int32_t* state_indices, int32_t num_slots, void* stream);
 
 /*
@@ -395,8 +416,10 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_slots(
  * uses on its mbarriers. Launches one CTA that waits, with that same wait, for
  * an mbarrier phase that nothing completes, giving up after about
  * `max_cycles` SM clock cycles (1 .. 4e9; the kernels use about 4e9, ~2 s).
- * When the wait gives up, *device_status becomes GDN_ERR_TIMEOUT and the CTA
- * exits normally: the context stays usable. GDN_OK would mean that the wait
+ * When the wait gives up, *device_status becomes GDN_ERR_TIMEOUT, the CTA
+ * records it in the sticky status that gdn_device_status reads (as every
+ * kernel of the library does when one of its waits gives up) and exits
+ * normally: the context stays usable. GDN_OK would mean that the wait
  * returned without its phase completing (a defect).
  *
  *   device_status  device int32 [1] (output).
@@ -404,6 +427,26 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked_slots(
  */
 GDN_API gdn_status_t gdn_selftest_bounded_wait(int32_t* device_status, int64_t max_cycles,
                                                void* stream);
+
+/*
+ * Failures that only the GPU can see. Every kernel of this library bounds its
+ * device-side waits (about two seconds); a wait that gives up makes its
+ * kernel stop without storing any unit of work it has not finished (the
+ * call's outputs and states are then undefined; nothing faults or hangs) and
+ * records GDN_ERR_TIMEOUT in a sticky device-side status of the library (one
+ * per CUDA context). The chunked prefill also reports it in its workspace
+ * (word 2).
+ *
+ * gdn_device_status enqueues, on `stream`, the read of that status into
+ * *status: GDN_OK, or the first failure recorded since the last clear. With
+ * clear = 1 the status is reset to GDN_OK after the read.
+ *
+ *   status  device int32 [1], 4-byte aligned (written by a kernel).
+ *   clear   0 or 1.
+ * NULL or misaligned status, or another clear value, is GDN_ERR_INVALID_ARG /
+ * GDN_ERR_ALIGNMENT. Allocates nothing.
+ */
+GDN_API gdn_status_t gdn_device_status(int32_t* status, int32_t clear, void* stream);
 
 /* Static description of a status code (never NULL). */
 GDN_API const char* gdn_status_string(gdn_status_t status);

@@ -106,7 +106,8 @@ def test_decode_validation(lib):
     assert decode(lib, S=None) == INVALID
     assert decode(lib, Hk=12) == INVALID                        # Hv % Hk
     assert decode(lib, qk_stride=1024) == INVALID               # stride < Hk * dk
-    assert decode(lib, l2=3) == INVALID
+    assert decode(lib, l2=4) == INVALID                         # unknown flag bit
+    assert decode(lib, l2=-1) == INVALID
     assert decode(lib, dk=96) == UNSUPPORTED
     assert decode(lib, dv=256, v_stride=8192) == UNSUPPORTED
     assert decode(lib, qk_stride=4100) == ALIGN
@@ -231,6 +232,13 @@ def test_state_slot_variants_validation(lib):
     bad = list(pre)
     bad[9] = 0
     assert p(*bad, A16, 8, None) == OK
+
+
+def test_device_status_validation(lib):
+    f = lib.gdn_device_status
+    assert f(None, 0, None) == INVALID
+    assert f(A16, 2, None) == INVALID
+    assert f(A16 + 2, 0, None) == ALIGN
 
 
 def test_selftest_bounded_wait_validation(lib):
