@@ -418,7 +418,9 @@ delta_decode_stream_kernel(const DecodeArgs p) {
           issued = i + kDecStages;
         }
       }
-      bulk_wait_all();
+      // The stores' shared-memory reads are done before the CTA exits; their
+      // global writes complete with the grid.
+      bulk_wait_read();
       // After an abort, units [i, issued) may still have loads landing in
       // their stages (distinct stages: fewer than kDecStages of them); their
       // phases are the latest armed ones, so waiting for them is exact.

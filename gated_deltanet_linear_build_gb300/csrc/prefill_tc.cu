@@ -609,6 +609,11 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (records_ok) {
       const uint32_t id64 = idesc_bf16_f32(128, 64);
       const uint32_t sah = taddr + 128, qt = smem_u32(sm + kS2_Q);
+      // Operand descriptors do not change across chunks: computed once, so
+      // that the issuing lane spends no time on them between MMAs.
+      uint64_t dq[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) dq[kk] = tile_desc(qt, 128, kk);
       for (int ci = 0; ci < nchunks; ++ci) {
         const uint32_t par = ci & 1;
         if (ci > 0 && !wait(bO1, (ci - 1) & 1)) break;
@@ -616,10 +621,14 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         bool ok = wait(bQ, par);
         ok = wait(bSr, par) && ok;
         if (ci > 0) ok = wait(bOr, (ci - 1) & 1) && ok;
+        // Issued once the X products are done, so that O1 fills the tensor
+        // pipe while the row warps compute Delta instead of delaying X.
+        ok = wait(bX, par) && ok;
         __syncwarp();
         fence_after_sync();
         if (ok && lane == 0) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 384, sah + 8 * kk, tile_desc(qt, 128, kk), id64, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 384, sah + 8 * kk, dq[kk], id64, kk > 0);
           mma_commit(bO1);
           issued = true;
           last_par = par;
@@ -694,6 +703,16 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       const uint32_t p = smem_u32(sm + kS2_P), kt = smem_u32(sm + kS2_K);
       // TMEM column of K step kk (16 tokens) of a Delta part based at `col`
       auto dcol = [&](int col, int kk) { return taddr + col + 8 * kk + (kk >= 2 ? 16 : 0); };
+      // Operand descriptors do not change across chunks: computed once, so
+      // that the issuing lane spends no time on them between MMAs.
+      uint64_t dw[8], dk4[4], dp4[4];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) dw[kk] = mn_desc(w, 128, kk);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        dk4[kk] = mn_desc(kt, 128, kk);
+        dp4[kk] = tile_desc(p, 64, kk);
+      }
       uint64_t* last = nullptr;
       uint32_t last_par = 0;
       for (int ci = 0; ci < nchunks; ++ci) {
@@ -705,8 +724,10 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         ok = wait(bSr, par) && ok;
         fence_after_sync();
         if (ok) {
-          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sah + 8 * kk, mn_desc(w, 128, kk), id128 | kTransB, kk > 0);
-          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sal + 8 * kk, mn_desc(w, 128, kk), id64 | kTransB, 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sah + 8 * kk, dw[kk], id128 | kTransB, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_bf16_tmem_a(taddr + 256, sal + 8 * kk, dw[kk], id64 | kTransB, 1);
           mma_commit(bX);
         }
         // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
@@ -718,10 +739,13 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           const uint32_t idk = id128 | kTransB;
           // A operands in TMEM: tokens 0-31 of each part in the hf = 0 columns,
           // tokens 32-63 in the hf = 1 columns (32 further on).
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(256, kk), mn_desc(kt, 128, kk), idk, 1);
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(272, kk), mn_desc(kt, 128, kk), idk, 1);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(256, kk), dk4[kk], idk, 1);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(272, kk), dk4[kk], idk, 1);
           mma_commit(bS);
-          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr + 448, dcol(320, kk), tile_desc(p, 64, kk), id64, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr + 448, dcol(320, kk), dp4[kk], id64, kk > 0);
           mma_commit(bO);
           last = bO;
           last_par = par;
