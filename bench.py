@@ -32,6 +32,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -66,9 +68,12 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--case", default="mix",
-                   choices=["mix", "conv_prefill", "conv_update", "decode", "prefill"],
-                   help="mix = the serving-mix sweep (the benchmark); the others time one "
-                        "hot-path call on its own workload shape (per-kernel studies, ncu)")
+                   choices=["mix", "conv_prefill", "conv_update", "decode", "prefill",
+                            "decode_step", "mixed_step"],
+                   help="mix = the serving-mix sweep (the benchmark); decode_step and "
+                        "mixed_step compare two ways of running one engine step (CUDA "
+                        "graphs over 24 layers); the others time one hot-path call on its "
+                        "own workload shape (per-kernel studies, ncu)")
     return p.parse_args(argv)
 
 
@@ -820,10 +825,156 @@ def run_case(args):
     return 0
 
 
+def time_graph(torch, stream, enqueue, steps, warmup):
+    """Capture ``enqueue()`` once as a CUDA graph on ``stream``; return the
+    average replay time in ms (CUDA events on that stream)."""
+    with torch.cuda.stream(stream):
+        enqueue()                              # eager run (kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        s_ev = torch.cuda.Event(enable_timing=True)
+        e_ev = torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+    return s_ev.elapsed_time(e_ev) / steps
+
+
+def run_step_case(args):
+    """decode_step: one decode step of 24 layers (N = 32 sequences), as
+    gdn_causal_conv1d_update + gdn_delta_rule_decode per layer against
+    gdn_decode_step_fused per layer. mixed_step: one 2048-token engine step of
+    24 layers carrying two prefill segments (1008 tokens each) and 32 decode
+    tokens, as one descriptor build + one conv prefill + one chunked prefill
+    per layer (the decode tokens ride the prefill calls as one-token
+    sequences) against the same prefill calls on the segments plus a conv
+    update + decode per layer for the decode tokens. Each variant is one CUDA
+    graph over distinct per-layer weights and states, replayed; inputs are
+    raw gate logits, q/k L2-normalised in the kernel."""
+    import torch
+    from gated_deltanet_linear_build_gb300 import build as B, gdn
+    B.build_library()
+    gdn.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    bf16 = torch.bfloat16
+    stream = torch.cuda.Stream(device=dev)
+
+    def randn(*shape, dtype=torch.float32, std=1.0):
+        return (torch.randn(shape, generator=g, device=dev) * std).to(dtype)
+
+    def views(y):
+        T = y.shape[0]
+        return (y[:, :HK * D].view(T, HK, D), y[:, HK * D:2 * HK * D].view(T, HK, D),
+                y[:, 2 * HK * D:].view(T, HV, D))
+
+    W = [randn(C, 4, dtype=bf16, std=0.5) for _ in range(LAYERS)]
+    out = {"case": args.case, "layers": LAYERS, "steps": args.steps}
+    if args.case == "decode_step":
+        N = N_SEQS
+        X = [randn(N, C, dtype=bf16) for _ in range(LAYERS)]
+        ZA = [randn(N, HV) for _ in range(LAYERS)]
+        ZB = [randn(N, HV) for _ in range(LAYERS)]
+        S = [randn(N, HV, D, D, std=0.02) for _ in range(LAYERS)]
+        ST = [[randn(N, C, 3, dtype=bf16) for _ in range(LAYERS)] for _ in range(2)]
+        Y = torch.empty((N, C), dtype=bf16, device=dev)
+        O = torch.empty((N, HV, D), dtype=bf16, device=dev)
+        par = [0]
+
+        def two_calls():
+            for l in range(LAYERS):
+                gdn.causal_conv1d_update(X[l], W[l], None, ST[0][l], Y)
+                q, k, v = views(Y)
+                gdn.delta_rule_decode(q, k, v, ZA[l], ZB[l], S[l], O, qk_l2norm=True,
+                                      gate_logits=True)
+
+        def fused():
+            # the fused step updates the conv state out of place: alternate buffers
+            for rep in range(2):
+                for l in range(LAYERS):
+                    gdn.decode_step_fused(X[l], W[l], None, ST[rep][l], ST[1 - rep][l], ZA[l],
+                                          ZB[l], S[l], O, Hk=HK, qk_l2norm=True,
+                                          gate_logits=True)
+
+        t2 = time_graph(torch, stream, two_calls, args.steps, args.warmup) / LAYERS
+        tf = time_graph(torch, stream, fused, args.steps, args.warmup) / (2 * LAYERS)
+        out.update(unit="us per layer-step (32 sequences)", two_calls=1e3 * t2,
+                   fused=1e3 * tf, fused_over_two_calls=tf / t2,
+                   delta_bytes_per_layer_step=decode_delta_bytes(),
+                   conv_bytes_per_layer_step=conv_update_bytes())
+    else:
+        seg, nd = 1008, N_SEQS
+        T = 2 * seg + nd
+        lens = [seg, seg] + [1] * nd
+        cu_list = [0]
+        for L in lens:
+            cu_list.append(cu_list[-1] + L)
+        cu_m = torch.tensor(cu_list, dtype=torch.int32, device=dev)
+        cu_p = torch.tensor([0, seg, 2 * seg], dtype=torch.int32, device=dev)
+        has_m = torch.ones(2 + nd, dtype=torch.uint8, device=dev)
+        has_p = torch.ones(2, dtype=torch.uint8, device=dev)
+        X = [randn(T, C, dtype=bf16) for _ in range(LAYERS)]
+        ZA = [randn(T, HV) for _ in range(LAYERS)]
+        ZB = [randn(T, HV) for _ in range(LAYERS)]
+        S = [randn(2 + nd, HV, D, D, std=0.02) for _ in range(LAYERS)]
+        ST = [randn(2 + nd, C, 3, dtype=bf16) for _ in range(LAYERS)]
+        Y = torch.empty((T, C), dtype=bf16, device=dev)
+        O = torch.empty((T, HV, D), dtype=bf16, device=dev)
+        ch = torch.empty((T // 8 + 2 + nd, 4), dtype=torch.int32, device=dev)
+        cnt = torch.empty(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(gdn.delta_rule_prefill_workspace_size(T, 2 + nd, HV, D, D),
+                         dtype=torch.uint8, device=dev)
+        P = 2 * seg
+
+        def mixed():
+            gdn.build_conv_chunks(cu_m, ch, cnt, chunk_tokens=8)
+            for l in range(LAYERS):
+                gdn.causal_conv1d_fwd(X[l], W[l], None, ST[l], has_m, cu_m, Y, chunks=ch,
+                                      num_chunks=cnt)
+                q, k, v = views(Y)
+                gdn.delta_rule_prefill_chunked(q, k, v, ZA[l], ZB[l], cu_m, S[l], has_m, O, ws,
+                                               qk_l2norm=True, gate_logits=True)
+
+        def separate():
+            gdn.build_conv_chunks(cu_p, ch, cnt, chunk_tokens=8)
+            for l in range(LAYERS):
+                gdn.causal_conv1d_fwd(X[l][:P], W[l], None, ST[l][:2], has_p, cu_p, Y[:P],
+                                      chunks=ch, num_chunks=cnt)
+                q, k, v = views(Y[:P])
+                gdn.delta_rule_prefill_chunked(q, k, v, ZA[l][:P], ZB[l][:P], cu_p, S[l][:2],
+                                               has_p, O[:P], ws, qk_l2norm=True,
+                                               gate_logits=True)
+                gdn.causal_conv1d_update(X[l][P:], W[l], None, ST[l][2:], Y[P:])
+                qd, kd, vd = views(Y[P:])
+                gdn.delta_rule_decode(qd, kd, vd, ZA[l][P:], ZB[l][P:], S[l][2:], O[P:],
+                                      qk_l2norm=True, gate_logits=True)
+
+        tm = time_graph(torch, stream, mixed, args.steps, args.warmup)
+        ts = time_graph(torch, stream, separate, args.steps, args.warmup)
+        out.update(unit="ms per 24-layer engine step", tokens=T, prefill_tokens=P,
+                   decode_tokens=nd, mixed=tm, separate=ts, mixed_over_separate=tm / ts,
+                   mixed_us_per_token_layer=1e3 * tm / (T * LAYERS),
+                   separate_us_per_token_layer=1e3 * ts / (T * LAYERS))
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.case in ("decode_step", "mixed_step"):
+        return run_step_case(args)
     if args.case != "mix":
         return run_case(args)
     return run_gdn(args)

@@ -59,15 +59,52 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return r;
 }
 
+// Buckets of the longest-first sequence order (chunk counts at or above the
+// last bucket share it; the order only decides which sequences start first).
+constexpr int kOrderBuckets = 1024;
+
+// order[0 .. n): the sequences by descending chunk count (empty ones last; the
+// order within one count is unspecified). A counting sort over chunk counts.
+__device__ void longest_first_order(const int32_t* __restrict__ cu, int n, int chunk,
+                                    int32_t* __restrict__ order, int* s_hist, bool valid) {
+  const int tid = threadIdx.x;
+  if (!valid) {   // malformed offsets: any permutation will do (nothing runs)
+    for (int s = tid; s < n; s += blockDim.x) order[s] = s;
+    return;
+  }
+  for (int b = tid; b < kOrderBuckets; b += blockDim.x) s_hist[b] = 0;
+  __syncthreads();
+  for (int s = tid; s < n; s += blockDim.x) {
+    const int c = (cu[s + 1] - cu[s] + chunk - 1) / chunk;
+    atomicAdd(&s_hist[min(c, kOrderBuckets - 1)], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {   // start of each bucket, largest counts first
+    int run = 0;
+    for (int b = kOrderBuckets - 1; b >= 0; --b) {
+      const int h = s_hist[b];
+      s_hist[b] = run;
+      run += h;
+    }
+  }
+  __syncthreads();
+  for (int s = tid; s < n; s += blockDim.x) {
+    const int c = (cu[s + 1] - cu[s] + chunk - 1) / chunk;
+    order[atomicAdd(&s_hist[min(c, kOrderBuckets - 1)], 1)] = s;
+  }
+}
+
 __global__ void __launch_bounds__(kBuildThreads)
 build_chunks_kernel(const int32_t* __restrict__ cu, int n, int chunk,
                     gdn_conv_chunk_t* __restrict__ out, int capacity,
-                    int32_t* __restrict__ num_chunks, int32_t* __restrict__ status) {
+                    int32_t* __restrict__ num_chunks, int32_t* __restrict__ status,
+                    int32_t* __restrict__ order) {
   __shared__ int s_off[kBuildThreads + 1];
   __shared__ int s_warp[32];
   __shared__ int s_total;
   __shared__ int s_bad;
   __shared__ unsigned long long s_count;
+  __shared__ int s_hist[kOrderBuckets];
   const int tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -87,6 +124,7 @@ build_chunks_kernel(const int32_t* __restrict__ cu, int n, int chunk,
   if (bad) atomicOr(&s_bad, 1);
   if (my) atomicAdd(&s_count, my);
   __syncthreads();
+  if (order) longest_first_order(cu, n, chunk, order, s_hist, !s_bad);
   if (s_bad || s_count > (unsigned long long)capacity) {
     if (tid == 0) {
       *num_chunks = 0;
@@ -612,9 +650,10 @@ conv_update_kernel(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
 
 gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
                                  gdn_conv_chunk_t* chunks, int32_t capacity,
-                                 int32_t* num_chunks, int32_t* status, cudaStream_t st) {
+                                 int32_t* num_chunks, int32_t* status, cudaStream_t st,
+                                 int32_t* order) {
   return check_launch(launch_pdl(build_chunks_kernel, dim3(1), dim3(kBuildThreads), 0, st, cu, n,
-                                chunk_tokens, chunks, capacity, num_chunks, status));
+                                chunk_tokens, chunks, capacity, num_chunks, status, order));
 }
 
 gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, const void* bias,

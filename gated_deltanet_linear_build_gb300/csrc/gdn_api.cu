@@ -303,6 +303,7 @@ gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride,
                                        flags);
   if (rc != GDN_OK) return rc;
   if (dk != dv) return GDN_ERR_UNSUPPORTED;
+  if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;   // one CTA per (sequence, head)
   return GDN_OK;
 }
 }  // namespace gdn

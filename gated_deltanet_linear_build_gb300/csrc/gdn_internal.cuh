@@ -278,9 +278,12 @@ gdn_status_t gather_status_prefill_tc(int32_t* out, int clear, int first, cudaSt
 
 // Launchers implemented in the kernel translation units. They assume their
 // arguments were validated by the C ABI layer.
+// order (device int32 [n] or nullptr): also write the sequences by descending
+// chunk count (longest first), for kernels that start long sequences first.
 gdn_status_t launch_build_chunks(const int32_t* cu, int32_t n, int32_t chunk_tokens,
                                  gdn_conv_chunk_t* chunks, int32_t capacity,
-                                 int32_t* num_chunks, int32_t* status, cudaStream_t st);
+                                 int32_t* num_chunks, int32_t* status, cudaStream_t st,
+                                 int32_t* order = nullptr);
 
 gdn_status_t launch_conv_fwd(const void* x, int64_t x_stride, const void* w, const void* bias,
                              void* conv_state, const uint8_t* has_init, const int32_t* cu,

@@ -62,14 +62,15 @@ __host__ __device__ constexpr size_t al256(size_t x) { return (x + 255) & ~size_
 
 struct TcLayout {
   int capacity;
-  size_t desc_off, rec_off, total;
+  size_t desc_off, order_off, rec_off, total;
 };
 
 __host__ __device__ inline TcLayout tc_layout(int T, int N, int Hv) {
   TcLayout L;
   L.capacity = T / kC + N + 1;
   L.desc_off = 256;
-  L.rec_off = L.desc_off + al256((size_t)L.capacity * sizeof(gdn_conv_chunk_t));
+  L.order_off = L.desc_off + al256((size_t)L.capacity * sizeof(gdn_conv_chunk_t));
+  L.rec_off = L.order_off + al256((size_t)N * sizeof(int32_t));
   L.total = L.rec_off + (size_t)L.capacity * Hv * kRecBytes;
   return L;
 }
@@ -492,7 +493,8 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                 int64_t qk_stride, const int32_t* __restrict__ cu, int T, int Hk,
                 float* __restrict__ S, const uint8_t* __restrict__ has_init,
                 __nv_bfloat16* __restrict__ o, int Hv, const unsigned char* __restrict__ records,
-                int32_t* __restrict__ hdr, const StateSlots slots) {
+                int32_t* __restrict__ hdr, const int32_t* __restrict__ order, int N,
+                const StateSlots slots) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const float* gk = reinterpret_cast<const float*>(sm + kS2_GK);
   const float4* us = reinterpret_cast<const float4*>(sm + kS2_U);
@@ -515,12 +517,16 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
   int* s_first = reinterpret_cast<int*>(sm + kS2_BAR + 108);
   int* s_fail = reinterpret_cast<int*>(sm + kS2_BAR + 112);
 
-  const int seq = blockIdx.x, h = blockIdx.y, gh = h / (Hv / Hk);
+  // CTA r * Hv + h runs head h of the r-th longest sequence, so that the
+  // long chains start in the first wave.
+  const int rank = blockIdx.x / Hv, h = blockIdx.x - rank * Hv, gh = h / (Hv / Hk);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = 32 * (warp & 3) + lane;   // row warps: S row (dv index) = TMEM lane
   const int hf = (warp >> 2) & 1;           // row warps: column / token half
   pdl_wait();
   pdl_trigger();
+  const int seq = order[rank];
+  if (seq < 0 || seq >= N) return;
   const int start = cu[seq], end = cu[seq + 1];
   if (start < 0 || end <= start || end > T) return;
   const int sslot = state_slot(slots, seq);
@@ -984,7 +990,8 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
   }();
   (void)attrs;
   if (cudaMemsetAsync(hdr + 2, 0, sizeof(int32_t), st) != cudaSuccess) return check_launch();
-  gdn_status_t rc = launch_build_chunks(cu, N, kC, desc, L.capacity, hdr, hdr + 1, st);
+  int32_t* order = reinterpret_cast<int32_t*>(ws + L.order_off);
+  gdn_status_t rc = launch_build_chunks(cu, N, kC, desc, L.capacity, hdr, hdr + 1, st, order);
   if (rc != GDN_OK) return rc;
   if ((rc = check_launch(launch_pdl(
            tc_chunk_kernel, dim3(L.capacity, Hv), dim3(kThreads), kS1_BYTES, st,
@@ -993,10 +1000,10 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
            Hv, flags, records, hdr))) != GDN_OK)
     return rc;
   return check_launch(launch_pdl(
-      tc_state_kernel, dim3(N, Hv), dim3(kThreads2), kS2_BYTES, st,
+      tc_state_kernel, dim3(N * Hv), dim3(kThreads2), kS2_BYTES, st,
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qk_stride, cu,
       T, Hk, S, has_init, static_cast<__nv_bfloat16*>(o), Hv, (const unsigned char*)records,
-      hdr, slots));
+      hdr, (const int32_t*)order, N, slots));
 }
 
 GDN_DEFINE_STATUS_GATHER(gather_status_prefill_tc)
