@@ -86,7 +86,13 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
         calls.append(seconds)
         return 2e-3, 5e-4, 0.0            # oracle seconds per decode / prefill token-layer
 
+    def fake_all_cores(seconds, pre, dec):
+        calls.append(seconds)
+        # four workers, each at the one-thread rate
+        return 4 * bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec), 4, 0.0
+
     monkeypatch.setattr(bench, "cpu_oracle_sample", fake_sample)
+    monkeypatch.setattr(bench, "cpu_oracle_all_cores", fake_all_cores)
     monkeypatch.delenv("WORLD_SIZE", raising=False)
     monkeypatch.delenv("RANK", raising=False)
     assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1"]) == 0
@@ -98,11 +104,21 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
                 "cpu_baseline", "e2e"):
         assert key in rec, key
     assert rec["impl"] == "reference" and rec["steps"] == 2 and rec["warmup"] == 1
-    assert len(calls) == 3                # one warm-up sample, then one per timed step
+    assert len(calls) == 3                # one warm-up sample, then one all-cores run per step
     from gated_deltanet_linear_build_gb300 import synth
     pre = int(sum(int(x) for x in synth.serving_mix_lengths(bench.rank_lengths_seed(0))))
     dec = bench.DECODE_STEPS * bench.N_SEQS
-    assert rec["value"] == pytest.approx(bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec))
+    assert rec["value"] == pytest.approx(4 * bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec))
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
+    assert rec["cpu_baseline"]["cores"] == 4
     assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_runs_on_every_core():
+    """The all-cores oracle leg spawns one worker per host core (no CUDA context
+    is inherited) and sums their rates; zero seconds means one sample each."""
+    import os
+    value, cores, wall = bench.cpu_oracle_all_cores(0.0, 100, 10)
+    assert cores == (os.cpu_count() or 1)
+    assert value > 0 and wall > 0
