@@ -154,30 +154,45 @@ constexpr int kFlagL2 = GDN_FLAG_QK_L2NORM;
 constexpr int kFlagGateLogits = GDN_FLAG_GATE_LOGITS;
 
 // Gate activation from raw logits: a = exp(-softplus(z)) (decay), b =
-// sigmoid(z) (write strength), with softplus(z) = max(z, 0) + log(1 + e^-|z|)
+// sigmoid(z) (write strength), on the hardware base-2 exponential and
+// logarithm (ex2.approx / lg2.approx: errors near 2^-22, far below what the
+// float32 state keeps): with u = log2 e,
+//   log2 a = -(max(z, 0) u + log2(1 + 2^(-|z| u))),   b = 1 / (1 + 2^(-z u)),
 // so that no intermediate overflows. Decays below 1e-30 act as 1e-30 in both
 // gate forms (the kernels work with log a).
-__device__ __forceinline__ float softplus_f(float z) {
-  return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 // log2 of the decay, clamped at log2(1e-30).
 __device__ __forceinline__ float gate_log2_decay(float x, bool logits) {
   constexpr float kLog2Min = -99.65784284662087f;   // log2(1e-30)
-  return logits ? fmaxf(-softplus_f(x) * 1.4426950408889634f, kLog2Min)
-                : log2f(fmaxf(x, 1e-30f));
+  constexpr float kLog2e = 1.4426950408889634f;
+  if (!logits) return log2f(fmaxf(x, 1e-30f));
+  const float sp2 = fmaxf(x, 0.f) * kLog2e + lg2_approx(1.0f + ex2_approx(-fabsf(x) * kLog2e));
+  return fmaxf(-sp2, kLog2Min);
 }
 // Natural log of the decay, clamped at ln(1e-30).
 __device__ __forceinline__ float gate_ln_decay(float x, bool logits) {
-  constexpr float kLnMin = -69.07755278982137f;     // ln(1e-30)
-  return logits ? fmaxf(-softplus_f(x), kLnMin) : logf(fmaxf(x, 1e-30f));
+  constexpr float kLn2 = 0.6931471805599453f;
+  return logits ? gate_log2_decay(x, true) * kLn2 : logf(fmaxf(x, 1e-30f));
 }
 // The decay itself (decode forms).
 __device__ __forceinline__ float gate_decay(float x, bool logits) {
-  return logits ? expf(-softplus_f(x)) : x;
+  return logits ? ex2_approx(gate_log2_decay(x, true)) : x;
 }
 // The write strength.
 __device__ __forceinline__ float gate_write(float x, bool logits) {
-  return logits ? 1.0f / (1.0f + expf(-x)) : x;
+  if (!logits) return x;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + ex2_approx(-x * 1.4426950408889634f)));
+  return r;
 }
 
 // ---------------------------------------------------------------------------
