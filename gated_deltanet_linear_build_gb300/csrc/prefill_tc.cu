@@ -737,9 +737,10 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
           mma_commit(bX);
         }
         // S += (Delta^T D) K (hi and lo passes);  O2^T = Delta^T P^T.
+        // The S update needs Delta and K only; O2 also needs P, whose copy
+        // may still be landing: waited for after the S update is issued.
         ok = wait(bDr, par);
         ok = wait(bK, par) && ok;
-        ok = wait(bP, par) && ok;
         fence_after_sync();
         if (ok) {
           const uint32_t idk = id128 | kTransB;
@@ -750,6 +751,12 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr, dcol(272, kk), dk4[kk], idk, 1);
           mma_commit(bS);
+          last = bS;   // the last commit so far (drained on exit)
+          last_par = par;
+          ok = wait(bP, par);
+          fence_after_sync();
+        }
+        if (ok) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) mma_bf16_tmem_a(taddr + 448, dcol(320, kk), dp4[kk], id64, kk > 0);
           mma_commit(bO);
@@ -839,13 +846,16 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
       // after this chunk's X MMAs, which wait for the S parts below.
       if (ci > 0) wait(bS, (ci - 1) & 1);
       wait(bW, par);
+      // The record's gates are read now (the buffer is refilled once this
+      // chunk's X products, which wait for the split below, are done); the
+      // per-token decay vectors are formed after the split, off its path.
       const float glast = gk[n - 1];
-      const float gamma_c = exp2_nonpos(glast);
       float* dkb = dks + 64 * par;
+      float g_t = 0.f, rk_t = 0.f, rq_t = 0.f;
       if (tid < 64) {
-        const bool in = tid < n;
-        dkb[tid] = in ? exp2_nonpos(glast - gk[tid]) * gk[64 + tid] : 0.f;
-        qs[64 * par + tid] = in ? exp2_nonpos(gk[tid]) * gk[128 + tid] : 0.f;
+        g_t = gk[tid];
+        rk_t = gk[64 + tid];
+        rq_t = gk[128 + tid];
       }
       // (b) this thread's half of S row i -> BF16 hi/lo pairs in TMEM (the
       // X and O1 MMAs' A operands), then S <- e^{g_last} S.
@@ -877,6 +887,12 @@ tc_state_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
         fence_before_sync();
         mbar_arrive(bSr);
+        if (tid < 64) {
+          const bool in = tid < n;
+          dkb[tid] = in ? exp2_nonpos(glast - g_t) * rk_t : 0.f;
+          qs[64 * par + tid] = in ? exp2_nonpos(g_t) * rq_t : 0.f;
+        }
+        const float gamma_c = exp2_nonpos(glast);
         // S <- e^{g_last} S, off the X MMAs' path: only this chunk's S update
         // (after Delta, whose barrier also orders this store) touches S next.
 #pragma unroll
