@@ -65,23 +65,27 @@ constexpr int kOrderBuckets = 1024;
 
 // order[0 .. n): the sequences by descending chunk count (empty ones last; the
 // order within one count is unspecified). A counting sort over chunk counts.
+// `capacity` bounds every sequence's chunk count, so only that many buckets
+// (at most kOrderBuckets) are used: a 2048-token step has about 36.
 __device__ void longest_first_order(const int32_t* __restrict__ cu, int n, int chunk,
-                                    int32_t* __restrict__ order, int* s_hist, bool valid) {
+                                    int capacity, int32_t* __restrict__ order, int* s_hist,
+                                    bool valid) {
   const int tid = threadIdx.x;
   if (!valid) {   // malformed offsets: any permutation will do (nothing runs)
     for (int s = tid; s < n; s += blockDim.x) order[s] = s;
     return;
   }
-  for (int b = tid; b < kOrderBuckets; b += blockDim.x) s_hist[b] = 0;
+  const int nb = max(1, min(kOrderBuckets, capacity + 1));
+  for (int b = tid; b < nb; b += blockDim.x) s_hist[b] = 0;
   __syncthreads();
   for (int s = tid; s < n; s += blockDim.x) {
     const int c = (cu[s + 1] - cu[s] + chunk - 1) / chunk;
-    atomicAdd(&s_hist[min(c, kOrderBuckets - 1)], 1);
+    atomicAdd(&s_hist[min(max(c, 0), nb - 1)], 1);
   }
   __syncthreads();
   if (tid == 0) {   // start of each bucket, largest counts first
     int run = 0;
-    for (int b = kOrderBuckets - 1; b >= 0; --b) {
+    for (int b = nb - 1; b >= 0; --b) {
       const int h = s_hist[b];
       s_hist[b] = run;
       run += h;
@@ -90,7 +94,7 @@ __device__ void longest_first_order(const int32_t* __restrict__ cu, int n, int c
   __syncthreads();
   for (int s = tid; s < n; s += blockDim.x) {
     const int c = (cu[s + 1] - cu[s] + chunk - 1) / chunk;
-    order[atomicAdd(&s_hist[min(c, kOrderBuckets - 1)], 1)] = s;
+    order[atomicAdd(&s_hist[min(max(c, 0), nb - 1)], 1)] = s;
   }
 }
 
@@ -124,7 +128,7 @@ build_chunks_kernel(const int32_t* __restrict__ cu, int n, int chunk,
   if (bad) atomicOr(&s_bad, 1);
   if (my) atomicAdd(&s_count, my);
   __syncthreads();
-  if (order) longest_first_order(cu, n, chunk, order, s_hist, !s_bad);
+  if (order) longest_first_order(cu, n, chunk, capacity, order, s_hist, !s_bad);
   if (s_bad || s_count > (unsigned long long)capacity) {
     if (tid == 0) {
       *num_chunks = 0;
