@@ -314,11 +314,17 @@ class Workload:
 
     def kind_sweep(self, kind):
         """Every call of one kind that a sweep makes, on the same buffers and
-        shapes, back to back (for per-kind launch durations)."""
+        shapes, back to back (for per-kind launch durations). The chunked
+        prefill calls run on the step's plan, remade before each step's calls
+        (so delta_prefill's time per call includes 1/24 of a plan)."""
+        from gated_deltanet_linear_build_gb300 import gdn
         st = self.stack
         for i, (cu, has, first, n, T) in enumerate(self.meta):
             if kind == "build_chunks":
-                st.build_chunks(cu)
+                st.build_chunks(cu, T)
+            elif kind == "delta_prefill":
+                # the step's plan, as the sweep makes it once per step
+                gdn.delta_rule_prefill_plan(cu, T, HV, D, D, st.workspace)
             for l in range(LAYERS):
                 if kind == "conv_prefill":
                     ch, cnt = self.step_chunks[i]
@@ -416,7 +422,7 @@ class E2EWorkload:
                 meta_ready = event(cin)
             compute.wait_event(meta_ready)
             with torch.cuda.stream(compute):
-                st.build_chunks(cu)
+                st.build_chunks(cu, T)
             xs, gs = wl.px[i], wl.pg[i]
             for l in range(LAYERS):
                 a, b = gs[l]

@@ -201,9 +201,10 @@ static gdn_status_t check_delta_common(const void* q, const void* k, int64_t qk_
                                        const void* v, int64_t v_stride, const float* a,
                                        const float* b, const float* S, const void* o,
                                        int32_t Hk, int32_t Hv, int32_t dk, int32_t dv,
-                                       int32_t flags) {
+                                       int32_t flags,
+                                       int32_t allowed = GDN_FLAG_QK_L2NORM | GDN_FLAG_GATE_LOGITS) {
   if (!q || !k || !v || !a || !b || !S || !o) return GDN_ERR_INVALID_ARG;
-  if (Hk <= 0 || Hv <= 0 || (flags & ~(GDN_FLAG_QK_L2NORM | GDN_FLAG_GATE_LOGITS)) != 0) return GDN_ERR_INVALID_ARG;
+  if (Hk <= 0 || Hv <= 0 || (flags & ~allowed) != 0) return GDN_ERR_INVALID_ARG;
   if (Hv % Hk != 0) return GDN_ERR_INVALID_ARG;
   if (!head_dim_ok(dk) || !head_dim_ok(dv)) return GDN_ERR_UNSUPPORTED;
   if (qk_stride < (int64_t)Hk * dk || v_stride < (int64_t)Hv * dv) return GDN_ERR_INVALID_ARG;
@@ -300,7 +301,8 @@ gdn_status_t check_prefill_args(const void* q, const void* k, int64_t qk_stride,
   }
   if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
   gdn_status_t rc = check_delta_common(q, k, qk_stride, v, v_stride, a, b, S, o, Hk, Hv, dk, dv,
-                                       flags);
+                                       flags,
+                                       GDN_FLAG_QK_L2NORM | GDN_FLAG_GATE_LOGITS | GDN_FLAG_PLANNED);
   if (rc != GDN_OK) return rc;
   if (dk != dv) return GDN_ERR_UNSUPPORTED;
   if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;   // one CTA per (sequence, head)
@@ -327,6 +329,22 @@ static gdn_status_t prefill_impl(const void* q, const void* k, int64_t qk_stride
   return launch_delta_prefill(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
                               has_initial_state, o, Hk, Hv, dk, dv, chunk, flags, workspace,
                               static_cast<cudaStream_t>(stream), slots);
+}
+
+gdn_status_t gdn_delta_rule_prefill_plan(const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                         int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
+                                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || N < 0 || Hv <= 0) return GDN_ERR_INVALID_ARG;
+  if (chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if (T == 0 || N == 0) return GDN_OK;
+  if (!cu_seqlens) return GDN_ERR_INVALID_ARG;
+  if (!head_dim_ok(dk) || !head_dim_ok(dv) || dk != dv) return GDN_ERR_UNSUPPORTED;
+  if ((int64_t)N * Hv > 0x7fffffff) return GDN_ERR_UNSUPPORTED;
+  const size_t need = prefill_workspace_bytes(T, N, Hv, dk, dv, chunk);
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_ALIGNMENT;
+  return launch_prefill_plan(cu_seqlens, N, T, Hv, dk, workspace,
+                             static_cast<cudaStream_t>(stream));
 }
 
 gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k, int64_t qk_stride,

@@ -152,6 +152,7 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 // ---------------------------------------------------------------------------
 constexpr int kFlagL2 = GDN_FLAG_QK_L2NORM;
 constexpr int kFlagGateLogits = GDN_FLAG_GATE_LOGITS;
+constexpr int kFlagPlanned = GDN_FLAG_PLANNED;
 
 // Gate activation from raw logits: a = exp(-softplus(z)) (decay), b =
 // sigmoid(z) (write strength), on the hardware base-2 exponential and
@@ -342,6 +343,13 @@ gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_strid
                                   int32_t Hv, int32_t dk, int32_t dv, int32_t chunk,
                                   int32_t flags, void* workspace, cudaStream_t st,
                                   StateSlots slots = {});
+
+// The chunk plan of a prefill (descriptors, and the longest-first order for
+// the tensor-core path) into the workspace.
+gdn_status_t launch_prefill_plan(const int32_t* cu, int32_t N, int32_t T, int32_t Hv,
+                                 int32_t dk, void* workspace, cudaStream_t st);
+gdn_status_t launch_prefill_tc_plan(const int32_t* cu, int32_t N, int32_t T, int32_t Hv,
+                                    void* workspace, cudaStream_t st);
 
 // Tensor-core (tcgen05) chunked prefill for dk = dv = 128.
 size_t prefill_tc_workspace_bytes(int32_t T, int32_t N, int32_t Hv);

@@ -294,8 +294,11 @@ gdn_status_t launch_prefill_t(const void* q, const void* k, int64_t qk_stride, c
   // Word 2 of the workspace header: the state pass's status. This state pass
   // has no device-side waits, so it always reports GDN_OK.
   if (cudaMemsetAsync(count + 2, 0, sizeof(int32_t), st) != cudaSuccess) return check_launch();
-  gdn_status_t rc = launch_build_chunks(cu, N, kChunk, desc, L.capacity, count, bstatus, st);
-  if (rc != GDN_OK) return rc;
+  gdn_status_t rc = GDN_OK;
+  if (!(flags & kFlagPlanned)) {
+    rc = launch_build_chunks(cu, N, kChunk, desc, L.capacity, count, bstatus, st);
+    if (rc != GDN_OK) return rc;
+  }
 
   constexpr int PK = DK + 1, PV = DV + 1, PT = kChunk + 1, PS = SL + 1;
   constexpr size_t smem1 =
@@ -330,6 +333,16 @@ size_t prefill_workspace_bytes(int32_t T, int32_t N, int32_t Hv, int32_t dk, int
   if (T < 0 || N < 0 || Hv <= 0 || dk <= 0 || dv <= 0 || chunk != kChunk) return 0;
   if (dk == 128 && dv == 128) return prefill_tc_workspace_bytes(T, N, Hv);
   return ws_layout(T, N, Hv, dk, dv).total;
+}
+
+gdn_status_t launch_prefill_plan(const int32_t* cu, int32_t N, int32_t T, int32_t Hv,
+                                 int32_t dk, void* workspace, cudaStream_t st) {
+  if (dk == 128) return launch_prefill_tc_plan(cu, N, T, Hv, workspace, st);
+  const WsLayout L = ws_layout(T, N, Hv, dk, dk);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* count = reinterpret_cast<int32_t*>(ws);
+  return launch_build_chunks(cu, N, kChunk, reinterpret_cast<gdn_conv_chunk_t*>(ws + L.desc_off),
+                             L.capacity, count, count + 1, st);
 }
 
 gdn_status_t launch_delta_prefill(const void* q, const void* k, int64_t qk_stride,

@@ -124,6 +124,9 @@ extern "C" gdn_status_t gdn_delta_rule_prefill_chunked_noalloc(
     int32_t chunk, int32_t flags, void* stream) {
   // Every argument check and the size limit come first, so a rejected call
   // touches no CUDA state at all (no context set-up, no symbol lookup).
+  // A plan (GDN_FLAG_PLANNED) would have to sit in the library's array,
+  // which the caller cannot address: this variant always builds its own.
+  if (flags & GDN_FLAG_PLANNED) return GDN_ERR_INVALID_ARG;
   bool nothing = false;
   gdn_status_t rc = check_prefill_args(q, k, qk_stride, v, v_stride, a, b, cu_seqlens, N, T, S,
                                        o, Hk, Hv, dk, dv, chunk, flags, &nothing);

@@ -988,6 +988,16 @@ size_t prefill_tc_workspace_bytes(int32_t T, int32_t N, int32_t Hv) {
   return tc_layout(T, N, Hv).total;
 }
 
+gdn_status_t launch_prefill_tc_plan(const int32_t* cu, int32_t N, int32_t T, int32_t Hv,
+                                    void* workspace, cudaStream_t st) {
+  const TcLayout L = tc_layout(T, N, Hv);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int32_t* hdr = reinterpret_cast<int32_t*>(ws);
+  return launch_build_chunks(cu, N, kC, reinterpret_cast<gdn_conv_chunk_t*>(ws + L.desc_off),
+                             L.capacity, hdr, hdr + 1, st,
+                             reinterpret_cast<int32_t*>(ws + L.order_off));
+}
+
 gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, const void* v,
                                int64_t v_stride, const float* a, const float* b,
                                const int32_t* cu, int32_t N, int32_t T, float* S,
@@ -1007,8 +1017,11 @@ gdn_status_t launch_prefill_tc(const void* q, const void* k, int64_t qk_stride, 
   (void)attrs;
   if (cudaMemsetAsync(hdr + 2, 0, sizeof(int32_t), st) != cudaSuccess) return check_launch();
   int32_t* order = reinterpret_cast<int32_t*>(ws + L.order_off);
-  gdn_status_t rc = launch_build_chunks(cu, N, kC, desc, L.capacity, hdr, hdr + 1, st, order);
-  if (rc != GDN_OK) return rc;
+  gdn_status_t rc = GDN_OK;
+  if (!(flags & kFlagPlanned)) {
+    rc = launch_build_chunks(cu, N, kC, desc, L.capacity, hdr, hdr + 1, st, order);
+    if (rc != GDN_OK) return rc;
+  }
   if ((rc = check_launch(launch_pdl(
            tc_chunk_kernel, dim3(L.capacity, Hv), dim3(kThreads), kS1_BYTES, st,
            static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(q), qk_stride,

@@ -26,6 +26,7 @@ GDN_ERR_TIMEOUT = -6
 # Option bits of the delta-rule calls' flags argument (GDN_FLAG_* in gdn.h).
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_GATE_LOGITS = 2
+GDN_FLAG_PLANNED = 4
 
 # Every symbol that include/gdn.h declares.
 EXPORTED_SYMBOLS = (
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "gdn_decode_step_fused",
     "gdn_delta_rule_prefill_workspace_size",
     "gdn_delta_rule_prefill_chunked",
+    "gdn_delta_rule_prefill_plan",
     "gdn_delta_rule_prefill_chunked_noalloc",
     "gdn_delta_rule_prefill_chunked_noalloc_status",
     "gdn_causal_conv1d_fwd_slots",
@@ -78,6 +80,8 @@ _SIGNATURES = {
     "gdn_delta_rule_prefill_chunked": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P, _I32,
                                                       _I32, _P, _P, _P, _I32, _I32, _I32, _I32,
                                                       _I32, _I32, _P, ctypes.c_size_t, _P]),
+    "gdn_delta_rule_prefill_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
+                                                   ctypes.c_size_t, _P]),
     "gdn_delta_rule_prefill_chunked_noalloc": (ctypes.c_int, [_P, _P, _I64, _P, _I64, _P, _P, _P,
                                                               _I32, _I32, _P, _P, _P, _I32, _I32,
                                                               _I32, _I32, _I32, _I32, _P]),
@@ -132,8 +136,9 @@ def _stream(stream=None):
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _flags(qk_l2norm: bool, gate_logits: bool) -> int:
-    return (GDN_FLAG_QK_L2NORM if qk_l2norm else 0) | (GDN_FLAG_GATE_LOGITS if gate_logits else 0)
+def _flags(qk_l2norm: bool, gate_logits: bool, planned: bool = False) -> int:
+    return ((GDN_FLAG_QK_L2NORM if qk_l2norm else 0) | (GDN_FLAG_GATE_LOGITS if gate_logits else 0)
+            | (GDN_FLAG_PLANNED if planned else 0))
 
 
 def _check(rc: int, fn: str):
@@ -217,8 +222,20 @@ def delta_rule_prefill_workspace_size(T: int, N: int, Hv: int, dk: int, dv: int,
     return int(_lib().gdn_delta_rule_prefill_workspace_size(T, N, Hv, dk, dv, chunk))
 
 
+def delta_rule_prefill_plan(cu_seqlens, T: int, Hv: int, dk: int, dv: int, workspace, *,
+                            chunk: int = 64, stream=None):
+    """Build the chunk plan of cu_seqlens into ``workspace`` once per engine
+    step; the step's prefill calls then pass planned=True and reuse it."""
+    N = cu_seqlens.numel() - 1
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib().gdn_delta_rule_prefill_plan(_ptr(cu_seqlens), N, T, Hv, dk, dv, chunk,
+                                            _ptr(workspace), nbytes, _stream(stream))
+    _check(rc, "gdn_delta_rule_prefill_plan")
+
+
 def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, o, workspace,
-                               *, chunk: int = 64, qk_l2norm: bool = False, gate_logits: bool = False, stream=None):
+                               *, chunk: int = 64, qk_l2norm: bool = False,
+                               gate_logits: bool = False, planned: bool = False, stream=None):
     """Chunked prefill over packed sequences. q, k [T, Hk, dk]; v [T, Hv, dv];
     a, b [T, Hv]; cu_seqlens [N+1]; S [N, Hv, dv, dk] (initial in, final out);
     has_initial_state uint8 [N] or None; o [T, Hv, dv]; workspace uint8 tensor
@@ -231,7 +248,7 @@ def delta_rule_prefill_chunked(q, k, v, a, b, cu_seqlens, S, has_initial_state, 
     rc = _lib().gdn_delta_rule_prefill_chunked(
         _ptr(q), _ptr(k), q.stride(0), _ptr(v), v.stride(0), _ptr(a), _ptr(b),
         _ptr(cu_seqlens), N, T, _ptr(S), _ptr(has_initial_state), _ptr(o), Hk, Hv, dk, dv,
-        chunk, _flags(qk_l2norm, gate_logits), _ptr(workspace), nbytes, _stream(stream))
+        chunk, _flags(qk_l2norm, gate_logits, planned), _ptr(workspace), nbytes, _stream(stream))
     _check(rc, "gdn_delta_rule_prefill_chunked")
 
 

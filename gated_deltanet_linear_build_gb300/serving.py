@@ -117,7 +117,7 @@ class SyntheticServingStack:
             h = self.embed[torch.from_numpy(toks).to(dev)].float()
             y = torch.empty((T, C), dtype=torch.bfloat16, device=dev)
             o = torch.empty((T, self.hv, self.d), dtype=torch.bfloat16, device=dev)
-            stack.build_chunks(cu_d)
+            stack.build_chunks(cu_d, T)
             for l in range(self.layers):
                 x = _rms_bf16(h).contiguous()
                 a, b = self._gates(l, x)

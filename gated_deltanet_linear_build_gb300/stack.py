@@ -8,8 +8,9 @@ tokens per step, 32 concurrent sequences):
 * a scheduler that packs prompts, in arrival order, into prefill steps of at
   most ``budget`` tokens (a prompt may be split across steps; its later part
   then continues from the carried conv_state and S);
-* per prefill step: the exact 8-token conv descriptors are built ONCE and
-  reused by every layer; per layer, the conv prefill over the descriptors and
+* per prefill step: the exact 8-token conv descriptors and the chunked
+  prefill's 64-token chunk plan are built ONCE and reused by every layer; per
+  layer, the conv prefill over the descriptors and
   the chunked delta-rule prefill on q/k/v read in place from the conv output
   (q/k L2-normalised and the gates activated from their logits inside the
   kernel);
@@ -27,8 +28,10 @@ import torch
 
 from . import gdn
 
-# Kernels enqueued by one gdn_delta_rule_prefill_chunked call.
-PREFILL_LAUNCHES = 3
+# Kernels enqueued by one gdn_delta_rule_prefill_chunked call on a planned
+# workspace (chunk kernel and state kernel); the plan itself is one more
+# launch per engine step.
+PREFILL_LAUNCHES = 2
 
 
 @dataclass
@@ -136,10 +139,12 @@ class GdnLayerStack:
         return cu, has, slots[0]
 
     # -- one call per kernel family -------------------------------------------
-    def build_chunks(self, cu_d):
-        """Exact 8-token conv descriptors of one prefill step (built once per step)."""
+    def build_chunks(self, cu_d, T: int):
+        """Exact 8-token conv descriptors and the chunked prefill's plan of one
+        prefill step of T tokens (built once per step, reused by every layer)."""
         gdn.build_conv_chunks(cu_d, self.chunks, self.num_chunks, chunk_tokens=8)
-        self.launches += 1
+        gdn.delta_rule_prefill_plan(cu_d, T, self.hv, self.d, self.d, self.workspace)
+        self.launches += 2
 
     def conv_prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, x, y,
                            chunks=None, num_chunks=None):
@@ -152,12 +157,13 @@ class GdnLayerStack:
         self.launches += 1
 
     def delta_prefill_layer(self, l: int, cu_d, has_d, first_slot: int, n: int, y, a, b, out):
-        """Layer l's chunked delta rule on q/k/v read in place from the conv output y."""
+        """Layer l's chunked delta rule on q/k/v read in place from the conv output
+        y, with the step's plan (build_chunks) already in the workspace."""
         sl = slice(first_slot, first_slot + n)
         q, k, v = self.qkv(y)
         gdn.delta_rule_prefill_chunked(q, k, v, a, b, cu_d, self.S[l][sl], has_d, out,
                                        self.workspace, qk_l2norm=True,
-                                       gate_logits=self.gate_logits)
+                                       gate_logits=self.gate_logits, planned=True)
         self.launches += PREFILL_LAUNCHES
 
     def conv_update_layer(self, l: int, x, y):
@@ -204,7 +210,7 @@ class GdnLayerStack:
         """
         tick = timer if timer is not None else (lambda kind, edge: None)
         tick("build_chunks", "start")
-        self.build_chunks(cu_d)
+        self.build_chunks(cu_d, int(xs[0].shape[0]))
         tick("build_chunks", "end")
         for l in range(self.layers):
             a, b = gates[l]

@@ -71,6 +71,9 @@ extern "C" {
  */
 #define GDN_FLAG_QK_L2NORM 1
 #define GDN_FLAG_GATE_LOGITS 2
+/* Chunked prefill only: the workspace already holds the call's chunk plan
+ * (gdn_delta_rule_prefill_plan), so the call skips building it. */
+#define GDN_FLAG_PLANNED 4
 
 /* Status codes. */
 typedef enum gdn_status_t {
@@ -255,7 +258,8 @@ GDN_API size_t gdn_delta_rule_prefill_workspace_size(int32_t T, int32_t N, int32
  *
  *   q, k, v, qk_stride, v_stride   as for decode, indexed by packed token t.
  *   a, b        float32 [T, Hv] (gates, or logits with GDN_FLAG_GATE_LOGITS).
- *   flags       GDN_FLAG_* bits, as for decode.
+ *   flags       GDN_FLAG_* bits, as for decode, plus GDN_FLAG_PLANNED (the
+ *               workspace holds this call's plan: gdn_delta_rule_prefill_plan).
  *   cu_seqlens  int32 [N + 1].
  *   S           float32 [N, Hv, dv, dk]: the initial state of sequence s where
  *               has_initial_state[s] != 0 (zeros otherwise), replaced by the
@@ -289,6 +293,32 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k
                                             void* stream);
 
 /*
+ * The chunk plan of a prefill step: the 64-token chunk descriptors of
+ * cu_seqlens (and, for dk = dv = 128, the order in which the state pass starts
+ * the sequences, longest first), written into `workspace` where
+ * gdn_delta_rule_prefill_chunked reads them. Source: "perf(gdn): dispatch
+ * exact causal-conv chunks", What changed (the step's descriptors are built
+ * once, uploaded once and reused by every layer): every layer of an engine
+ * step runs the prefill on the same cu_seqlens, so one plan per step serves
+ * them all, each call passing GDN_FLAG_PLANNED.
+ *
+ *   cu_seqlens, N, T, Hv, dk, dv, chunk   as for gdn_delta_rule_prefill_chunked.
+ *   workspace, workspace_bytes            the workspace those calls will use
+ *                                         (at least the size they need).
+ * Host-side validation as for the prefill (same status codes). One kernel
+ * launch; device-side failures (malformed cu_seqlens) are reported in
+ * workspace word 1, and every planned call then leaves its state and outputs
+ * untouched. A call with GDN_FLAG_PLANNED must use the same cu_seqlens
+ * contents, N, T, Hv, dk, dv and chunk as the plan (not checked), and the plan
+ * region of the workspace (everything but the chunk records) must not have
+ * been overwritten in between; calls without the flag rebuild the plan.
+ */
+GDN_API gdn_status_t gdn_delta_rule_prefill_plan(const int32_t* cu_seqlens, int32_t N, int32_t T,
+                                                 int32_t Hv, int32_t dk, int32_t dv,
+                                                 int32_t chunk, void* workspace,
+                                                 size_t workspace_bytes, void* stream);
+
+/*
  * The chunked prefill above, for callers that cannot allocate device memory.
  * (The pages describe no such variant; it exists for integration only.)
  *
@@ -301,7 +331,8 @@ GDN_API gdn_status_t gdn_delta_rule_prefill_chunked(const void* q, const void* k
  * process exits.
  *
  * Arguments, results and layouts are those of gdn_delta_rule_prefill_chunked,
- * minus workspace / workspace_bytes. Sizes whose workspace
+ * minus workspace / workspace_bytes; GDN_FLAG_PLANNED is GDN_ERR_INVALID_ARG
+ * here (a plan would have to live in the library's array). Sizes whose workspace
  * (gdn_delta_rule_prefill_workspace_size) exceeds 64 MiB are rejected with
  * GDN_ERR_WORKSPACE before anything is enqueued (for example, 2 x 512 tokens
  * with 32 v-heads of width 128 fit; 2 x 1024 tokens do not).

@@ -106,7 +106,7 @@ def test_decode_validation(lib):
     assert decode(lib, S=None) == INVALID
     assert decode(lib, Hk=12) == INVALID                        # Hv % Hk
     assert decode(lib, qk_stride=1024) == INVALID               # stride < Hk * dk
-    assert decode(lib, l2=4) == INVALID                         # unknown flag bit
+    assert decode(lib, l2=8) == INVALID                         # unknown flag bit
     assert decode(lib, l2=-1) == INVALID
     assert decode(lib, dk=96) == UNSUPPORTED
     assert decode(lib, dv=256, v_stride=8192) == UNSUPPORTED
@@ -156,6 +156,22 @@ def test_prefill_noalloc_validation_before_any_cuda_call(lib):
     assert prefill_noalloc(lib, T=2048) == WORKSPACE             # beyond the 64 MiB array
     assert prefill_noalloc(lib, T=0) == OK
     assert lib.gdn_delta_rule_prefill_chunked_noalloc_status(None, None) == INVALID
+
+
+def test_prefill_plan_validation(lib):
+    f = lib.gdn_delta_rule_prefill_plan
+    need = lib.gdn_delta_rule_prefill_workspace_size(2048, 2, 32, 128, 128, 64)
+    ws = A16 * 16
+    assert f(None, 2, 2048, 32, 128, 128, 64, ws, need, None) == INVALID
+    assert f(A16, 2, 2048, 32, 128, 128, 32, ws, need, None) == UNSUPPORTED
+    assert f(A16, 2, 2048, 32, 128, 64, 64, ws, need, None) == UNSUPPORTED
+    assert f(A16, 2, 2048, 32, 128, 128, 64, ws, need - 1, None) == WORKSPACE
+    assert f(A16, 2, 2048, 32, 128, 128, 64, ws + 16, need, None) == ALIGN
+    assert f(A16, 2, 0, 32, 128, 128, 64, ws, need, None) == OK
+    # the planned bit belongs to the prefill only
+    assert prefill(lib, l2=8) == INVALID                        # unknown flag bit
+    assert decode(lib, l2=4) == INVALID
+    assert prefill_noalloc(lib, l2=4) == INVALID
 
 
 def test_decode_step_fused_validation(lib):

@@ -335,3 +335,28 @@ def test_prefill_slow_decay_state_precision(G):
     d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
     o, S = prefill_gpu(G, d)
     check_prefill(d, o, S)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_plan_reused_by_two_layers_equals_unplanned(G, D):
+    """One chunk plan per engine step ("perf(gdn): dispatch exact causal-conv
+    chunks", What changed: built once per step, reused by every layer): two
+    calls with different inputs on one plan give the bytes of two calls that
+    build their own, which the tests above hold against the oracle."""
+    lengths = [130, 1, 64, 0, 257, 7]
+    cases = [synth.delta_case(60 + i, lengths, 2, 4, D, D, s0_std=0.05) for i in range(2)]
+    T, N = cases[0]["T"], cases[0]["N"]
+    cu = dev(cases[0]["cu_seqlens"])
+    ws_plan = torch.empty(G.delta_rule_prefill_workspace_size(T, N, 4, D, D), dtype=torch.uint8,
+                          device="cuda")
+    G.delta_rule_prefill_plan(cu, T, 4, D, D, ws_plan)
+    for c in cases:
+        ref_o, ref_S = prefill_gpu(G, c)
+        S = dev(c["S0"].reshape(N, 4, D, D))
+        o = torch.full((T, 4, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        G.delta_rule_prefill_chunked(bf16_dev(c["q"]), bf16_dev(c["k"]), bf16_dev(c["v"]),
+                                     dev(c["a"]), dev(c["b"]), cu, S, dev(c["has_initial_state"]),
+                                     o, ws_plan, planned=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(S.view(torch.int32), ref_S.view(torch.int32))
