@@ -344,37 +344,66 @@ class Workload:
 
 
 class E2EWorkload:
-    """The same sweep fed from pinned host memory: every layer input (x, a, b,
-    and the step's cu_seqlens / flags) is copied host->device before its layer
-    and every layer output o is copied device->host after it.
+    """The same sweep fed from pinned host memory: every layer's inputs (x and
+    the gate logits z_a, z_b) and every step's cu_seqlens / flags are copied
+    host->device, and every layer's output o is copied device->host.
 
-    The copies run on two side streams, inputs on one and outputs on the
-    other, so that they overlap the kernels of other layers. Events order
-    them: in prefill steps per layer (a layer's kernels wait for that layer's
-    input copies, its output copy waits for its kernels, and the layer's next
-    step waits for the previous copy out of the same output buffer); in decode
-    steps per engine step."""
+    The link to the host, not the copy engines, bounds these copies (a single
+    cudaMemcpyAsync already reaches it), so each copy is as large as the data
+    allows: a prefill layer's x | z_a | z_b sit back to back in one device
+    buffer and arrive in one copy; a decode step's inputs for all 24 layers
+    arrive in one copy, and its 24 outputs, back to back in one device buffer,
+    leave in one copy. Inputs and outputs run on two side streams so that they
+    overlap the kernels of other layers; events order them per layer in
+    prefill steps (each (step, layer) has its own input and output buffers, so
+    no kernel waits for a previous copy out) and per engine step in decode
+    steps (outputs alternate between two buffers)."""
 
     def __init__(self, wl: Workload):
         torch = wl.torch
         self.wl = wl
-        pin = dict(pin_memory=True)
-        self.hpx = [torch.randn((STEP_TOKENS, C), dtype=torch.bfloat16).pin_memory()
+        dev = wl.meta[0][0].device
+        u8, bf16, f32 = torch.uint8, torch.bfloat16, torch.float32
+        per_tok = C * 2 + 2 * HV * 4              # x (BF16) | z_a | z_b (float32)
+
+        def host_bytes(nbytes):
+            # random BF16 values, so that any float32 read of them is finite
+            return torch.randn(nbytes // 2, dtype=bf16).view(u8).pin_memory()
+
+        def views(buf, n, base=0):
+            x = buf[base:base + n * C * 2].view(bf16).view(n, C)
+            o = base + n * C * 2
+            za = buf[o:o + n * HV * 4].view(f32).view(n, HV)
+            zb = buf[o + n * HV * 4:o + 2 * n * HV * 4].view(f32).view(n, HV)
+            return x, za, zb
+
+        self.hp = [host_bytes(STEP_TOKENS * per_tok) for _ in range(LAYERS)]
+        self.dp = []                               # [step][layer] -> (buf, x, za, zb, o)
+        for (_cu, _has, _first, _n, T) in wl.meta:
+            row = []
+            for _ in range(LAYERS):
+                buf = torch.empty(T * per_tok, dtype=u8, device=dev)
+                row.append((buf,) + views(buf, T) +
+                           (torch.empty((T, HV, D), dtype=bf16, device=dev),))
+            self.dp.append(row)
+        self.hpo = [torch.empty((STEP_TOKENS, HV, D), dtype=bf16).pin_memory()
                     for _ in range(LAYERS)]
-        self.hpa = [torch.rand((STEP_TOKENS, HV), **pin) for _ in range(LAYERS)]
-        self.hpb = [torch.rand((STEP_TOKENS, HV), **pin) for _ in range(LAYERS)]
-        self.hdx = [torch.randn((N_SEQS, C), dtype=torch.bfloat16).pin_memory()
-                    for _ in range(LAYERS)]
-        self.hda = [torch.rand((N_SEQS, HV), **pin) for _ in range(LAYERS)]
-        self.hdb = [torch.rand((N_SEQS, HV), **pin) for _ in range(LAYERS)]
-        self.hpo = [torch.empty((STEP_TOKENS, HV, D), dtype=torch.bfloat16, **pin)
-                    for _ in range(LAYERS)]
-        self.hdo = [torch.empty((N_SEQS, HV, D), dtype=torch.bfloat16, **pin)
-                    for _ in range(LAYERS)]
+        per_layer = N_SEQS * per_tok
+        self.hd = host_bytes(LAYERS * per_layer)
+        self.dd = []                               # [decode step] -> (buf, xs, gates)
+        for _ in range(DECODE_STEPS):
+            buf = torch.empty(LAYERS * per_layer, dtype=u8, device=dev)
+            xs, gs = [], []
+            for l in range(LAYERS):
+                x, za, zb = views(buf, N_SEQS, l * per_layer)
+                xs.append(x)
+                gs.append((za, zb))
+            self.dd.append((buf, xs, gs))
+        self.dout = [torch.empty((LAYERS, N_SEQS, HV, D), dtype=bf16, device=dev)
+                     for _ in range(2)]
+        self.hdo = torch.empty((LAYERS, N_SEQS, HV, D), dtype=bf16).pin_memory()
         self.hcu = [m[0].cpu().pin_memory() for m in wl.meta]
         self.hhas = [m[1].cpu().pin_memory() for m in wl.meta]
-        dev = wl.meta[0][0].device
-        self.do2 = [torch.empty_like(t) for t in wl.do]
         self.cin = torch.cuda.Stream(device=dev)
         self.cout = torch.cuda.Stream(device=dev)
         self.h2d = 0
@@ -387,32 +416,12 @@ class E2EWorkload:
         cin, cout = self.cin, self.cout
         cin.wait_stream(compute)
         cout.wait_stream(compute)
-        out_free = {}          # output buffer -> event: its last copy-out is done
         h2d = d2h = 0
 
         def event(s):
             ev = torch.cuda.Event()
             ev.record(s)
             return ev
-
-        def run_layer(key, inputs, kernels, out_dev, out_host):
-            nonlocal h2d, d2h
-            with torch.cuda.stream(cin):
-                for dst, src in inputs:
-                    dst.copy_(src, non_blocking=True)
-                    h2d += src.numel() * src.element_size()
-                ready = event(cin)
-            compute.wait_event(ready)
-            if key in out_free:
-                compute.wait_event(out_free[key])
-            with torch.cuda.stream(compute):
-                kernels()
-                done = event(compute)
-            with torch.cuda.stream(cout):
-                cout.wait_event(done)
-                out_host.copy_(out_dev, non_blocking=True)
-                d2h += out_dev.numel() * out_dev.element_size()
-                out_free[key] = event(cout)
 
         for i, (cu, has, first, n, T) in enumerate(wl.meta):
             with torch.cuda.stream(cin):
@@ -423,43 +432,38 @@ class E2EWorkload:
             compute.wait_event(meta_ready)
             with torch.cuda.stream(compute):
                 st.build_chunks(cu, T)
-            xs, gs = wl.px[i], wl.pg[i]
             for l in range(LAYERS):
-                a, b = gs[l]
-                y, o = wl.py[l][:T], wl.po[l][:T]
-                run_layer(("p", l),
-                          [(xs[l], self.hpx[l][:T]), (a, self.hpa[l][:T]), (b, self.hpb[l][:T])],
-                          lambda l=l, a=a, b=b, y=y, o=o, xl=xs[l], cu=cu, has=has, first=first,
-                          n=n: st.prefill_layer(l, cu, has, first, n, xl, a, b, y, o),
-                          o, self.hpo[l][:T])
-        # Decode steps move their inputs and outputs one engine step at a time
-        # (one event each way per step, so that consecutive layers' kernels
-        # keep their programmatic dependent launches); the step's outputs
-        # alternate between two buffer sets, so a step never waits for the
-        # previous step's outputs to leave.
-        outs = [wl.do, self.do2]
+                buf, x, za, zb, o = self.dp[i][l]
+                with torch.cuda.stream(cin):
+                    buf.copy_(self.hp[l][:buf.numel()], non_blocking=True)
+                    h2d += buf.numel()
+                    ready = event(cin)
+                compute.wait_event(ready)
+                with torch.cuda.stream(compute):
+                    st.prefill_layer(l, cu, has, first, n, x, za, zb, wl.py[l][:T], o)
+                    done = event(compute)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(done)
+                    self.hpo[l][:T].copy_(o, non_blocking=True)
+                    d2h += o.numel() * o.element_size()
         free = [None, None]
         for j in range(DECODE_STEPS):
-            xs, gs = wl.dx[j], wl.dg[j]
+            buf, xs, gs = self.dd[j]
             with torch.cuda.stream(cin):
-                for l in range(LAYERS):
-                    for dst, src in ((xs[l], self.hdx[l]), (gs[l][0], self.hda[l]),
-                                     (gs[l][1], self.hdb[l])):
-                        dst.copy_(src, non_blocking=True)
-                        h2d += src.numel() * src.element_size()
+                buf.copy_(self.hd, non_blocking=True)
+                h2d += buf.numel()
                 ready = event(cin)
             compute.wait_event(ready)
-            ob = outs[j & 1]
+            ob = self.dout[j & 1]
             if free[j & 1] is not None:
                 compute.wait_event(free[j & 1])
             with torch.cuda.stream(compute):
-                st.decode_step(xs, gs, wl.dy, ob)
+                st.decode_step(xs, gs, wl.dy, [ob[l] for l in range(LAYERS)])
                 done = event(compute)
             with torch.cuda.stream(cout):
                 cout.wait_event(done)
-                for l in range(LAYERS):
-                    self.hdo[l].copy_(ob[l], non_blocking=True)
-                    d2h += ob[l].numel() * ob[l].element_size()
+                self.hdo.copy_(ob, non_blocking=True)
+                d2h += ob.numel() * ob.element_size()
                 free[j & 1] = event(cout)
         compute.wait_stream(cin)
         compute.wait_stream(cout)
@@ -741,9 +745,10 @@ def run_gdn(args):
                       "h2d_bytes_per_step": e2.h2d, "d2h_bytes_per_step": e2.d2h,
                       "ms_per_step": ms2,
                       "path": "C-ABI calls on buffers copied from/to pinned host memory "
-                              "(cudaMemcpyAsync per tensor on two side streams, ordered per "
-                              "layer in prefill steps and per engine step in decode steps, "
-                              "overlapping the kernels of other layers), inside the graph"}
+                              "(one cudaMemcpyAsync per prefill layer each way and per decode "
+                              "step each way, on two side streams, ordered per layer in "
+                              "prefill steps and per engine step in decode steps, overlapping "
+                              "the kernels of other layers), inside the graph"}
 
     if rank == 0 and not args.no_cpu_baseline:
         pd, pp, spent = cpu_oracle_sample(args.cpu_seconds / 2)
