@@ -232,6 +232,15 @@ def test_decode_full_size(G):
     check_decode(d, o, S)
 
 
+def test_decode_many_sequences(G):
+    # 101 sequences: 6,464 state units of 64 rows over the persistent CTAs, so
+    # each CTA walks its stage ring several times over (and the units do not
+    # divide evenly among the CTAs).
+    d = synth.delta_case(43, [1] * 101, 16, 32, 128, 128, s0_std=0.02)
+    o, S = decode_gpu(G, d, qk_l2norm=True)
+    check_decode(d, o, S, qk_l2norm=True)
+
+
 def test_decode_strided_views_and_l2norm(G):
     d = synth.delta_case(41, [1] * 32, 16, 32, 128, 128, s0_std=0.02, normed_qk=False)
     o, S = decode_gpu(G, d, qk_l2norm=True, strided=True)
@@ -335,6 +344,30 @@ def test_prefill_slow_decay_state_precision(G):
     d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
     o, S = prefill_gpu(G, d)
     check_prefill(d, o, S)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_long_sequences(G, D):
+    # Chains of 79 and 50 chunk steps plus a one-token sequence (8,192 tokens),
+    # with slowly decaying gates so that the state carries information across
+    # the whole chain; few heads keep the float64 oracle within seconds.
+    lengths = [5000, 3191, 1]
+    d = synth.delta_case(56, lengths, 2, 4, D, D, s0_std=0.05)
+    d["has_initial_state"] = np.array([1, 0, 1], np.uint8)
+    rng = np.random.default_rng(57)
+    z = rng.standard_normal(d["a"].shape) - 4.5
+    d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
+    o, S = prefill_gpu(G, d)
+    check_prefill(d, o, S)
+
+
+def test_conv_long_sequences(G):
+    # 8,000-token sequence (1,000 exact 8-token chunks) beside short ones.
+    lengths = [8000, 191, 1]
+    case = synth.conv_case(33, lengths, 256, bias=True)
+    case["has_initial_state"] = np.array([1, 0, 1], np.uint8)
+    y, st = conv_gpu(G, case)
+    check_conv(case, y, st)
 
 
 @pytest.mark.parametrize("D", [128, 64])
