@@ -343,6 +343,21 @@ class Workload:
                     st.delta_decode_layer(l, self.dy[l], a, b, self.do[l])
 
 
+E2E_BYTES_PER_TOKEN = C * 2 + 2 * HV * 4      # x (BF16) | z_a | z_b (float32)
+
+
+def packed_layer_inputs(buf, n, base=0):
+    """Views of one layer's inputs for n tokens packed back to back in the byte
+    tensor ``buf`` from byte ``base``: x BF16 [n, C], then z_a and z_b float32
+    [n, HV]; together they cover n * E2E_BYTES_PER_TOKEN bytes."""
+    import torch
+    x = buf[base:base + n * C * 2].view(torch.bfloat16).view(n, C)
+    o = base + n * C * 2
+    za = buf[o:o + n * HV * 4].view(torch.float32).view(n, HV)
+    zb = buf[o + n * HV * 4:o + 2 * n * HV * 4].view(torch.float32).view(n, HV)
+    return x, za, zb
+
+
 class E2EWorkload:
     """The same sweep fed from pinned host memory: every layer's inputs (x and
     the gate logits z_a, z_b) and every step's cu_seqlens / flags are copied
@@ -363,19 +378,12 @@ class E2EWorkload:
         torch = wl.torch
         self.wl = wl
         dev = wl.meta[0][0].device
-        u8, bf16, f32 = torch.uint8, torch.bfloat16, torch.float32
-        per_tok = C * 2 + 2 * HV * 4              # x (BF16) | z_a | z_b (float32)
+        u8, bf16 = torch.uint8, torch.bfloat16
+        per_tok = E2E_BYTES_PER_TOKEN
 
         def host_bytes(nbytes):
             # random BF16 values, so that any float32 read of them is finite
             return torch.randn(nbytes // 2, dtype=bf16).view(u8).pin_memory()
-
-        def views(buf, n, base=0):
-            x = buf[base:base + n * C * 2].view(bf16).view(n, C)
-            o = base + n * C * 2
-            za = buf[o:o + n * HV * 4].view(f32).view(n, HV)
-            zb = buf[o + n * HV * 4:o + 2 * n * HV * 4].view(f32).view(n, HV)
-            return x, za, zb
 
         self.hp = [host_bytes(STEP_TOKENS * per_tok) for _ in range(LAYERS)]
         self.dp = []                               # [step][layer] -> (buf, x, za, zb, o)
@@ -383,7 +391,7 @@ class E2EWorkload:
             row = []
             for _ in range(LAYERS):
                 buf = torch.empty(T * per_tok, dtype=u8, device=dev)
-                row.append((buf,) + views(buf, T) +
+                row.append((buf,) + packed_layer_inputs(buf, T) +
                            (torch.empty((T, HV, D), dtype=bf16, device=dev),))
             self.dp.append(row)
         self.hpo = [torch.empty((STEP_TOKENS, HV, D), dtype=bf16).pin_memory()
@@ -395,7 +403,7 @@ class E2EWorkload:
             buf = torch.empty(LAYERS * per_layer, dtype=u8, device=dev)
             xs, gs = [], []
             for l in range(LAYERS):
-                x, za, zb = views(buf, N_SEQS, l * per_layer)
+                x, za, zb = packed_layer_inputs(buf, N_SEQS, l * per_layer)
                 xs.append(x)
                 gs.append((za, zb))
             self.dd.append((buf, xs, gs))

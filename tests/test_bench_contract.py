@@ -122,3 +122,36 @@ def test_cpu_baseline_runs_on_every_core():
     value, cores, wall = bench.cpu_oracle_all_cores(0.0, 100, 10)
     assert cores == (os.cpu_count() or 1)
     assert value > 0 and wall > 0
+
+
+def test_packed_layer_inputs_tile_the_buffer_without_overlap():
+    # The end-to-end leg copies each layer's x | z_a | z_b as one buffer: the
+    # three views must cover it exactly, in order, aligned for the kernels'
+    # 16-byte row loads, at a prefill layer's size and at a decode layer's
+    # offset inside a step buffer.
+    import torch
+    per_tok = bench.E2E_BYTES_PER_TOKEN
+    assert per_tok == bench.C * 2 + 2 * bench.HV * 4
+    for n, base, layers in ((2048, 0, 1), (1810, 0, 1), (bench.N_SEQS, 0, 3)):
+        buf = torch.zeros(layers * n * per_tok, dtype=torch.uint8)
+        spans = []
+        for l in range(layers):
+            x, za, zb = bench.packed_layer_inputs(buf, n, base + l * n * per_tok)
+            assert x.shape == (n, bench.C) and x.dtype == torch.bfloat16
+            assert za.shape == zb.shape == (n, bench.HV) and za.dtype == torch.float32
+            for t in (x, za, zb):
+                assert t.is_contiguous()
+                off = t.data_ptr() - buf.data_ptr()
+                assert off % 16 == 0
+                spans.append((off, off + t.numel() * t.element_size()))
+        assert spans[0][0] == 0 and spans[-1][1] == buf.numel()
+        assert all(a[1] == b[0] for a, b in zip(spans, spans[1:]))
+        # writes through the views land in disjoint bytes
+        for l in range(layers):
+            x, za, zb = bench.packed_layer_inputs(buf, n, base + l * n * per_tok)
+            x.fill_(1.0)
+            za.fill_(2.0)
+            zb.fill_(3.0)
+        for l in range(layers):
+            x, za, zb = bench.packed_layer_inputs(buf, n, base + l * n * per_tok)
+            assert bool((x == 1.0).all()) and bool((za == 2.0).all()) and bool((zb == 3.0).all())
