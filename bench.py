@@ -346,6 +346,18 @@ class Workload:
 E2E_BYTES_PER_TOKEN = C * 2 + 2 * HV * 4      # x (BF16) | z_a | z_b (float32)
 
 
+def compact(obj, digits=6):
+    """The JSON line's numbers to `digits` significant digits (floats only), so
+    that the whole line stays short enough to survive a log tail."""
+    if isinstance(obj, float):
+        return float(f"{obj:.{digits}g}")
+    if isinstance(obj, dict):
+        return {k: compact(v, digits) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return [compact(v, digits) for v in obj]
+    return obj
+
+
 def packed_layer_inputs(buf, n, base=0):
     """Views of one layer's inputs for n tokens packed back to back in the byte
     tensor ``buf`` from byte ``base``: x BF16 [n, C], then z_a and z_b float32
@@ -482,11 +494,8 @@ class E2EWorkload:
 # CPU baseline: the oracle on a bounded sample of the same workload
 # ----------------------------------------------------------------------------
 
-CPU_SAMPLE = ("oracle (float64 numpy) on one layer: a 32-sequence decode step (conv update + "
-              "delta decode) and a 2x128-token prefill slice (conv + sequential delta rule, 32 "
-              "heads), repeated for the sample time; per-token-layer times scaled to the "
-              "24-layer mix; run on one thread, and on every host core at once (one worker "
-              "process per core, each timing its own share)")
+CPU_SAMPLE = ("float64 oracle, one layer: 32-seq decode step + 2x128-token prefill slice, "
+              "per-token-layer times scaled to the 24-layer mix; 1 thread and 1 process/core")
 
 
 def cpu_oracle_sample(seconds: float):
@@ -583,7 +592,7 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    print(json.dumps(compact(line)), flush=True)
     return 0
 
 
@@ -715,11 +724,9 @@ def run_gdn(args):
                    "prefill_tokens": wl.prefill_tokens, "decode_tokens": wl.decode_tokens,
                    "prefill_steps": len(wl.steps), "step_tokens": STEP_TOKENS,
                    "conv_channels": C, "v_heads": HV, "qk_heads": HK, "head_dim": D,
-                   "l2": "inputs larger than L2 (about 11 GB of distinct layer inputs per sweep)",
-                   "timing": "CUDA graph of one sweep (kernels only) replayed K-1 times on the "
-                             "timing stream, then the same calls once more grouped by kernel kind "
-                             "(one graph per kind, CUDA events around each group: per-kind launch "
-                             "durations); CUDA events on the stream bracket all K",
+                   "l2": "inputs > L2 (~11 GB of distinct layer inputs per sweep)",
+                   "timing": "sweep graph x (K-1) + per-kind graphs x 1, CUDA events on the "
+                             "launch stream around all K",
                    "parallelism": f"dp{world} (independent sequences per GPU)"},
         "roofline": roofline,
         "kernels": kernels,
@@ -752,11 +759,8 @@ def run_gdn(args):
         out["e2e"] = {"value": tokens_all / (ms2 / 1e3), "unit": "tokens/s",
                       "h2d_bytes_per_step": e2.h2d, "d2h_bytes_per_step": e2.d2h,
                       "ms_per_step": ms2,
-                      "path": "C-ABI calls on buffers copied from/to pinned host memory "
-                              "(one cudaMemcpyAsync per prefill layer each way and per decode "
-                              "step each way, on two side streams, ordered per layer in "
-                              "prefill steps and per engine step in decode steps, overlapping "
-                              "the kernels of other layers), inside the graph"}
+                      "path": "C-ABI calls; pinned host <-> device copies in the graph, one per "
+                              "prefill layer and per decode step each way, two side streams"}
 
     if rank == 0 and not args.no_cpu_baseline:
         pd, pp, spent = cpu_oracle_sample(args.cpu_seconds / 2)
@@ -768,7 +772,7 @@ def run_gdn(args):
             "sample": CPU_SAMPLE, "one_thread_value": one,
             "cpu_seconds": spent + wall * cores}
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        print(json.dumps(compact(out)), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0

@@ -108,7 +108,9 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
     from gated_deltanet_linear_build_gb300 import synth
     pre = int(sum(int(x) for x in synth.serving_mix_lengths(bench.rank_lengths_seed(0))))
     dec = bench.DECODE_STEPS * bench.N_SEQS
-    assert rec["value"] == pytest.approx(4 * bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec))
+    # the line's numbers carry six significant digits
+    assert rec["value"] == pytest.approx(4 * bench.mix_tokens_per_s(2e-3, 5e-4, pre, dec),
+                                         rel=1e-5)
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["cpu_baseline"]["value"] == rec["value"]
     assert rec["cpu_baseline"]["cores"] == 4
     assert rec["e2e"] == {"value": rec["value"], "unit": rec["unit"], "h2d_bytes_per_step": 0,
@@ -155,3 +157,10 @@ def test_packed_layer_inputs_tile_the_buffer_without_overlap():
         for l in range(layers):
             x, za, zb = bench.packed_layer_inputs(buf, n, base + l * n * per_tok)
             assert bool((x == 1.0).all()) and bool((za == 2.0).all()) and bool((zb == 3.0).all())
+
+
+def test_compact_keeps_six_significant_digits():
+    out = bench.compact({"a": 276078.08729208616, "b": [0.9070752634563363, 3],
+                         "c": {"d": 1e-7 / 3, "e": "text", "f": None, "g": True}})
+    assert out == {"a": 276078.0, "b": [0.907075, 3],
+                   "c": {"d": 3.33333e-08, "e": "text", "f": None, "g": True}}
