@@ -380,11 +380,18 @@ class E2EWorkload:
     allows: a prefill layer's x | z_a | z_b sit back to back in one device
     buffer and arrive in one copy; a decode step's inputs for all 24 layers
     arrive in one copy, and its 24 outputs, back to back in one device buffer,
-    leave in one copy. Inputs and outputs run on two side streams so that they
-    overlap the kernels of other layers; events order them per layer in
-    prefill steps (each (step, layer) has its own input and output buffers, so
-    no kernel waits for a previous copy out) and per engine step in decode
-    steps (outputs alternate between two buffers)."""
+    leave in one copy.
+
+    The prefill inputs are double-buffered across sweeps, as an engine
+    prefetches its next batch: each sweep's graph copies the NEXT sweep's
+    prefill inputs into the other buffer set, a slice after each decode step's
+    inputs on the same input stream, which runs ahead of the kernels; so they
+    cross the link while this sweep's kernels run (sweep() with ``own=True``
+    also copies its own prefill inputs first, layer by layer, as the first
+    timed sweep must). A stream of their own for the prefetch measured slower:
+    the decode steps' inputs then queued behind 34 MB copies. Outputs leave on
+    a second side stream as soon as their layer (prefill) or engine step
+    (decode) is done; decode outputs alternate between two buffers."""
 
     def __init__(self, wl: Workload):
         torch = wl.torch
@@ -398,14 +405,13 @@ class E2EWorkload:
             return torch.randn(nbytes // 2, dtype=bf16).view(u8).pin_memory()
 
         self.hp = [host_bytes(STEP_TOKENS * per_tok) for _ in range(LAYERS)]
-        self.dp = []                               # [step][layer] -> (buf, x, za, zb, o)
-        for (_cu, _has, _first, _n, T) in wl.meta:
-            row = []
-            for _ in range(LAYERS):
-                buf = torch.empty(T * per_tok, dtype=u8, device=dev)
-                row.append((buf,) + packed_layer_inputs(buf, T) +
-                           (torch.empty((T, HV, D), dtype=bf16, device=dev),))
-            self.dp.append(row)
+        # dp[set][step][layer] -> (buf, x, za, zb); po[step][layer] -> o
+        self.dp = [[[(lambda buf: (buf,) + packed_layer_inputs(buf, T))(
+                        torch.empty(T * per_tok, dtype=u8, device=dev))
+                     for _ in range(LAYERS)] for (_cu, _has, _first, _n, T) in wl.meta]
+                   for _ in range(2)]
+        self.po = [[torch.empty((T, HV, D), dtype=bf16, device=dev) for _ in range(LAYERS)]
+                   for (_cu, _has, _first, _n, T) in wl.meta]
         self.hpo = [torch.empty((STEP_TOKENS, HV, D), dtype=bf16).pin_memory()
                     for _ in range(LAYERS)]
         per_layer = N_SEQS * per_tok
@@ -429,13 +435,15 @@ class E2EWorkload:
         self.h2d = 0
         self.d2h = 0
 
-    def sweep(self, compute):
-        """Enqueue one sweep; ``compute`` is the stream the kernels go to (and
-        the one being captured)."""
+    def sweep(self, compute, use, prefetch, own):
+        """Enqueue one sweep on ``compute`` (the stream being captured): the
+        prefill kernels read input set ``use``; the next sweep's prefill inputs
+        go to set ``prefetch``; with ``own`` this sweep first copies its own
+        prefill inputs into set ``use``. Leaves the sweep's bytes in h2d, d2h."""
         wl, st, torch = self.wl, self.wl.stack, self.wl.torch
         cin, cout = self.cin, self.cout
-        cin.wait_stream(compute)
-        cout.wait_stream(compute)
+        for s in (cin, cout):
+            s.wait_stream(compute)
         h2d = d2h = 0
 
         def event(s):
@@ -443,6 +451,9 @@ class E2EWorkload:
             ev.record(s)
             return ev
 
+        # the next sweep's prefill inputs, a slice per decode step (their
+        # buffers were last read by the previous sweep's kernels)
+        items = [(i, l) for i in range(len(wl.meta)) for l in range(LAYERS)]
         for i, (cu, has, first, n, T) in enumerate(wl.meta):
             with torch.cuda.stream(cin):
                 cu.copy_(self.hcu[i], non_blocking=True)
@@ -453,12 +464,14 @@ class E2EWorkload:
             with torch.cuda.stream(compute):
                 st.build_chunks(cu, T)
             for l in range(LAYERS):
-                buf, x, za, zb, o = self.dp[i][l]
-                with torch.cuda.stream(cin):
-                    buf.copy_(self.hp[l][:buf.numel()], non_blocking=True)
-                    h2d += buf.numel()
-                    ready = event(cin)
-                compute.wait_event(ready)
+                buf, x, za, zb = self.dp[use][i][l]
+                o = self.po[i][l]
+                if own:
+                    with torch.cuda.stream(cin):
+                        buf.copy_(self.hp[l][:buf.numel()], non_blocking=True)
+                        h2d += buf.numel()
+                        ready = event(cin)
+                    compute.wait_event(ready)
                 with torch.cuda.stream(compute):
                     st.prefill_layer(l, cu, has, first, n, x, za, zb, wl.py[l][:T], o)
                     done = event(compute)
@@ -473,6 +486,11 @@ class E2EWorkload:
                 buf.copy_(self.hd, non_blocking=True)
                 h2d += buf.numel()
                 ready = event(cin)
+                lo, hi = len(items) * j // DECODE_STEPS, len(items) * (j + 1) // DECODE_STEPS
+                for (pi, pl) in items[lo:hi]:
+                    pbuf = self.dp[prefetch][pi][pl][0]
+                    pbuf.copy_(self.hp[pl][:pbuf.numel()], non_blocking=True)
+                    h2d += pbuf.numel()
             compute.wait_event(ready)
             ob = self.dout[j & 1]
             if free[j & 1] is not None:
@@ -485,8 +503,8 @@ class E2EWorkload:
                 self.hdo.copy_(ob, non_blocking=True)
                 d2h += ob.numel() * ob.element_size()
                 free[j & 1] = event(cout)
-        compute.wait_stream(cin)
-        compute.wait_stream(cout)
+        for s in (cin, cout):
+            compute.wait_stream(s)
         self.h2d, self.d2h = h2d, d2h
 
 
@@ -737,30 +755,44 @@ def run_gdn(args):
     if not args.no_e2e:
         e2 = E2EWorkload(wl)
         with torch.cuda.stream(stream):
-            e2.sweep(stream)
+            e2.sweep(stream, use=0, prefetch=1, own=True)      # eager warm run
         torch.cuda.synchronize()
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            e2.sweep(stream)
+        # g_first copies its own prefill inputs (set 0) and prefetches set 1;
+        # then g_a (reads 1, prefetches 0) and g_b (reads 0, prefetches 1)
+        # alternate. Every timed sweep's inputs cross the link inside the
+        # timed region: the first sweep's before its kernels, the others'
+        # during the sweep before them.
+        graphs, moved = {}, {}
+        for name, use, pre, own in (("first", 0, 1, True), ("a", 1, 0, False),
+                                    ("b", 0, 1, False)):
+            graphs[name] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graphs[name], stream=stream):
+                e2.sweep(stream, use=use, prefetch=pre, own=own)
+            moved[name] = (e2.h2d, e2.d2h)
+        order = ["first"] + ["a" if k % 2 else "b" for k in range(1, args.steps)]
         with torch.cuda.stream(stream):
             for _ in range(max(1, args.warmup)):
-                g2.replay()
+                for name in ("first", "a", "b"):
+                    graphs[name].replay()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         s2, e2_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             s2.record(stream)
-            for _ in range(args.steps):
-                g2.replay()
+            for name in order:
+                graphs[name].replay()
             e2_.record(stream)
         torch.cuda.synchronize()
         ms2 = reduce_over_ranks(s2.elapsed_time(e2_) / args.steps, "max", dist, dev)
         out["e2e"] = {"value": tokens_all / (ms2 / 1e3), "unit": "tokens/s",
-                      "h2d_bytes_per_step": e2.h2d, "d2h_bytes_per_step": e2.d2h,
+                      "h2d_bytes_per_step": sum(moved[n][0] for n in order) // len(order),
+                      "d2h_bytes_per_step": sum(moved[n][1] for n in order) // len(order),
                       "ms_per_step": ms2,
                       "path": "C-ABI calls; pinned host <-> device copies in the graph, one per "
-                              "prefill layer and per decode step each way, two side streams"}
+                              "prefill layer and per decode step each way; the next sweep's "
+                              "prefill inputs are prefetched during this sweep's decode steps "
+                              "(double buffered); the first timed sweep copies its own"}
 
     if rank == 0 and not args.no_cpu_baseline:
         pd, pp, spent = cpu_oracle_sample(args.cpu_seconds / 2)
