@@ -114,50 +114,85 @@ constexpr int kS1_TF = 16384;
 constexpr int kS1_TWH = kS1_AF, kS1_TWL = kS1_AF + 8192;
 constexpr int kS1_TUH = 16384, kS1_TUL = 24576;
 
+// TC consecutive floats from shared memory (TC = 2 or 4).
+template <int TC>
+__device__ __forceinline__ void lds_vec(const float* p, float (&v)[TC]) {
+  if constexpr (TC == 4) {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  } else {
+    const float2 f = *reinterpret_cast<const float2*>(p);
+    v[0] = f.x; v[1] = f.y;
+  }
+}
+
 // One distance of the blocked triangular inverse: for the tiles (i, j = i - D),
 // R_ij = sum_{s in [16 j, 16 i)} A[16 i + rr][s] Tm[s][16 j + cc], then
-// Tm_ij = -D_i R_ij. Each thread owns 2 (4 - D) outputs and carries them as
-// independent accumulators; trip counts are compile-time.
-template <int D>
+// Tm_ij = -D_i R_ij. Thread t owns a TR x TC piece of one tile, accumulated in
+// registers from vector loads (TR rows of A and four rows of Tm per step of
+// four s), with the pieces sized so that nearly every thread has one at every
+// distance (2 x 4 on 96 threads, 1 x 4 and 1 x 2 on 128); trip counts are
+// compile-time.
+template <int D, int TR, int TC>
 __device__ __forceinline__ void tm_offdiag(const float* __restrict__ Af, float* __restrict__ Tf,
                                            float* __restrict__ Rs, int tid) {
-  constexpr int kOut = 2 * (4 - D);
-  float acc[kOut];
+  constexpr int kPerRow = 16 / TC, kPerTile = (16 / TR) * kPerRow;
+  constexpr int kPieces = (4 - D) * kPerTile;
+  const int blk = tid / kPerTile, t = tid - blk * kPerTile;
+  const int i = D + blk, jb = i - D;
+  const int r0 = TR * (t / kPerRow), c0 = TC * (t - (t / kPerRow) * kPerRow);
+  if (tid < kPieces) {
+    float acc[TR][TC];
 #pragma unroll
-  for (int q = 0; q < kOut; ++q) acc[q] = 0.f;
+    for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
-  for (int s4 = 0; s4 < 16 * D; s4 += 4) {
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
 #pragma unroll
-    for (int q = 0; q < kOut; ++q) {
-      const int e = tid + 128 * q;
-      const int blk = e >> 8, i = D + blk, jb = i - D, rr = (e >> 4) & 15, cc = e & 15;
+    for (int s4 = 0; s4 < 16 * D; s4 += 4) {
       const int s0 = 16 * jb + s4;
-      const float4 a4 = *reinterpret_cast<const float4*>(Af + (16 * i + rr) * 68 + s0);
-      acc[q] = fmaf(a4.x, Tf[(s0 + 0) * 64 + 16 * jb + cc], acc[q]);
-      acc[q] = fmaf(a4.y, Tf[(s0 + 1) * 64 + 16 * jb + cc], acc[q]);
-      acc[q] = fmaf(a4.z, Tf[(s0 + 2) * 64 + 16 * jb + cc], acc[q]);
-      acc[q] = fmaf(a4.w, Tf[(s0 + 3) * 64 + 16 * jb + cc], acc[q]);
-    }
-  }
+      float a[TR][4], tv[4][TC];
 #pragma unroll
-  for (int q = 0; q < kOut; ++q) Rs[tid + 128 * q] = acc[q];
+      for (int rr = 0; rr < TR; ++rr) lds_vec<4>(Af + (16 * i + r0 + rr) * 68 + s0, a[rr]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lds_vec<TC>(Tf + (s0 + e) * 64 + 16 * jb + c0, tv[e]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+          for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = fmaf(a[rr][e], tv[e][cc], acc[rr][cc]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc) Rs[blk * 256 + (r0 + rr) * 16 + c0 + cc] = acc[rr][cc];
+  }
   __syncthreads();
+  if (tid < kPieces) {
+    float acc[TR][TC];
 #pragma unroll
-  for (int q = 0; q < kOut; ++q) acc[q] = 0.f;
+    for (int rr = 0; rr < TR; ++rr)
 #pragma unroll
-  for (int k2 = 0; k2 < 16; ++k2) {
+      for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = 0.f;
 #pragma unroll
-    for (int q = 0; q < kOut; ++q) {
-      const int e = tid + 128 * q;
-      const int blk = e >> 8, i = D + blk, rr = (e >> 4) & 15, cc = e & 15;
-      acc[q] = fmaf(Tf[(16 * i + rr) * 64 + 16 * i + k2], Rs[blk * 256 + k2 * 16 + cc], acc[q]);
+    for (int k4 = 0; k4 < 16; k4 += 4) {
+      float d[TR][4], rv[4][TC];
+#pragma unroll
+      for (int rr = 0; rr < TR; ++rr) lds_vec<4>(Tf + (16 * i + r0 + rr) * 64 + 16 * i + k4, d[rr]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lds_vec<TC>(Rs + blk * 256 + (k4 + e) * 16 + c0, rv[e]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+          for (int cc = 0; cc < TC; ++cc) acc[rr][cc] = fmaf(d[rr][e], rv[e][cc], acc[rr][cc]);
     }
-  }
 #pragma unroll
-  for (int q = 0; q < kOut; ++q) {
-    const int e = tid + 128 * q;
-    const int blk = e >> 8, i = D + blk, jb = i - D, rr = (e >> 4) & 15, cc = e & 15;
-    Tf[(16 * i + rr) * 64 + 16 * jb + cc] = -acc[q];
+    for (int rr = 0; rr < TR; ++rr)
+#pragma unroll
+      for (int cc = 0; cc < TC; ++cc)
+        Tf[(16 * i + r0 + rr) * 64 + 16 * jb + c0 + cc] = -acc[rr][cc];
   }
   __syncthreads();
 }
@@ -336,9 +371,9 @@ tc_chunk_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __rest
     }
   }
   __syncthreads();
-  tm_offdiag<1>(Af, Tf, Rs, tid);
-  tm_offdiag<2>(Af, Tf, Rs, tid);
-  tm_offdiag<3>(Af, Tf, Rs, tid);
+  tm_offdiag<1, 2, 4>(Af, Tf, Rs, tid);
+  tm_offdiag<2, 1, 4>(Af, Tf, Rs, tid);
+  tm_offdiag<3, 1, 2>(Af, Tf, Rs, tid);
   // B tiles: column s of Tm diag(b e^g rk) and of Tm diag(b), split hi/lo, as
   // MN-major tiles (N = r, K = s): eight consecutive r per 16 bytes. The W-side
   // tiles go to the (now free) A area at once; the U-side ones are held in
