@@ -69,11 +69,12 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--case", default="mix",
                    choices=["mix", "conv_prefill", "conv_update", "decode", "prefill",
-                            "decode_step", "mixed_step"],
+                            "decode_step", "mixed_step", "decode_units"],
                    help="mix = the serving-mix sweep (the benchmark); decode_step and "
                         "mixed_step compare two ways of running one engine step (CUDA "
-                        "graphs over 24 layers); the others time one hot-path call on its "
-                        "own workload shape (per-kernel studies, ncu)")
+                        "graphs over 24 layers); decode_units times the decode over a "
+                        "range of sequence counts (units per CTA); the others time one "
+                        "hot-path call on its own workload shape (per-kernel studies, ncu)")
     return p.parse_args(argv)
 
 
@@ -943,6 +944,54 @@ def time_graph(torch, stream, enqueue, steps, warmup):
     return s_ev.elapsed_time(e_ev) / steps
 
 
+def run_decode_units(args):
+    """The decode (d = 128, 32 v-heads over 16 k-heads, gate logits, q/k L2
+    norm) at several sequence counts, as graphs of 48 calls cycling over
+    states whose total exceeds L2: one JSON line per count with the 64-row
+    units per persistent CTA, us per launch and the fraction of the measured
+    HBM peak."""
+    import torch
+    from gated_deltanet_linear_build_gb300 import build as B, gdn
+    B.build_library()
+    gdn.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak = load_peaks()[0]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    stream = torch.cuda.Stream(device=dev)
+    calls = 48
+    for n in (16, 19, 24, 32, 38, 48, 57, 64):
+        per = decode_delta_bytes(n)
+        nsets = max(3, int(400e6 // per) + 1)
+        sets = []
+        for _ in range(nsets):
+            y = torch.randn((n, C), generator=g, device=dev).to(torch.bfloat16)
+            sets.append((y, torch.randn((n, HV), generator=g, device=dev),
+                         torch.randn((n, HV), generator=g, device=dev),
+                         torch.randn((n, HV, D, D), generator=g, device=dev) * 0.02,
+                         torch.empty((n, HV, D), dtype=torch.bfloat16, device=dev)))
+
+        def enqueue():
+            for i in range(calls):
+                y, a, b, S, o = sets[i % nsets]
+                gdn.delta_rule_decode(y[:, :HK * D].view(n, HK, D),
+                                      y[:, HK * D:2 * HK * D].view(n, HK, D),
+                                      y[:, 2 * HK * D:].view(n, HV, D), a, b, S, o,
+                                      qk_l2norm=True, gate_logits=True)
+        us = time_graph(torch, stream, enqueue, max(1, args.steps // 4), args.warmup) \
+            * 1e3 / calls
+        units = n * HV * 2
+        print(json.dumps(compact({"case": "decode_units", "seqs": n, "units": units,
+                                  "units_per_cta": units / sms, "us_per_launch": us,
+                                  "achieved_gbs": per / us / 1e3,
+                                  "frac": per / us / 1e3 / hbm_peak})), flush=True)
+        del sets
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_step_case(args):
     """decode_step: one decode step of 24 layers (N = 32 sequences), as
     gdn_causal_conv1d_update + gdn_delta_rule_decode per layer against
@@ -1070,6 +1119,8 @@ def main(argv=None):
         return run_reference(args)
     if args.case in ("decode_step", "mixed_step"):
         return run_step_case(args)
+    if args.case == "decode_units":
+        return run_decode_units(args)
     if args.case != "mix":
         return run_case(args)
     return run_gdn(args)
