@@ -241,6 +241,15 @@ def test_decode_many_sequences(G):
     check_decode(d, o, S, qk_l2norm=True)
 
 
+@pytest.mark.parametrize("n", [1, 3])
+def test_decode_small_batches(G, n):
+    # 64 or 192 state units: fewer units than persistent CTAs, or one or two
+    # per CTA.
+    d = synth.delta_case(44 + n, [1] * n, 16, 32, 128, 128, s0_std=0.02)
+    o, S = decode_gpu(G, d)
+    check_decode(d, o, S)
+
+
 def test_decode_strided_views_and_l2norm(G):
     d = synth.delta_case(41, [1] * 32, 16, 32, 128, 128, s0_std=0.02, normed_qk=False)
     o, S = decode_gpu(G, d, qk_l2norm=True, strided=True)
@@ -342,6 +351,18 @@ def test_prefill_slow_decay_state_precision(G):
     rng = np.random.default_rng(55)
     z = rng.standard_normal(d["a"].shape) - 4.5
     d["a"] = np.exp(-np.logaddexp(0.0, z)).astype(np.float32)
+    o, S = prefill_gpu(G, d)
+    check_prefill(d, o, S)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_prefill_many_short_sequences(G, D):
+    # 200 sequences of 1-9 tokens (and a few empty ones): 800 one-chunk chains,
+    # several waves of state CTAs in longest-first order with many ties.
+    rng = np.random.default_rng(58)
+    lengths = [int(x) for x in rng.integers(0, 10, size=200)]
+    d = synth.delta_case(59, lengths, 2, 4, D, D, s0_std=0.05)
+    d["has_initial_state"] = (np.arange(len(lengths)) % 3 != 0).astype(np.uint8)
     o, S = prefill_gpu(G, d)
     check_prefill(d, o, S)
 
