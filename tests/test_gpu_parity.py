@@ -382,6 +382,15 @@ def test_prefill_long_sequences(G, D):
     check_prefill(d, o, S)
 
 
+def test_conv_prefill_large_step(G):
+    # 16,384 tokens x 8192 channels in one call (2,048 descriptors of 8 tokens):
+    # each persistent CTA walks several times the runs of the 2048-token step.
+    case = synth.conv_case(34, [9000, 4000, 3000, 384], 8192, bias=True)
+    case["has_initial_state"] = np.array([1, 0, 1, 1], np.uint8)
+    y, st = conv_gpu(G, case)
+    check_conv(case, y, st)
+
+
 def test_conv_long_sequences(G):
     # 8,000-token sequence (1,000 exact 8-token chunks) beside short ones.
     lengths = [8000, 191, 1]
