@@ -355,6 +355,15 @@ def test_prefill_slow_decay_state_precision(G):
     check_prefill(d, o, S)
 
 
+def test_prefill_large_step(G):
+    # 8,192 tokens of 4 sequences, all 32 v-heads over 16 k-heads, d = 128: 128
+    # chains of up to 47 chunk steps, a 130-record-per-head workspace.
+    d = synth.delta_case(60, [3000, 2500, 2000, 692], 16, 32, 128, 128, s0_std=0.02)
+    d["has_initial_state"] = np.array([1, 0, 1, 0], np.uint8)
+    o, S = prefill_gpu(G, d)
+    check_prefill(d, o, S)
+
+
 @pytest.mark.parametrize("D", [128, 64])
 def test_prefill_many_short_sequences(G, D):
     # 200 sequences of 1-9 tokens (and a few empty ones): 800 one-chunk chains,
